@@ -1,0 +1,211 @@
+"""CPU oracle for the MoE route / dispatch / combine path (numpy front end).
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg (``bench.py --impl reference`` and the
+``cpu_baseline`` object) may import this package. The product path never does:
+the CUDA library and its binding share no code with it.
+
+The arithmetic lives in ``moe_oracle.c`` (plain, single-threaded C); this module
+only marshals numpy arrays. Page citations are in the C source:
+  [PMC] "Efficient and portable mixture-of-experts communication"
+  [DBO] "Dual Batch Overlap"
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from .build import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build()
+        L = C.CDLL(path)
+        P = C.c_void_p
+        i32, i64 = C.c_int32, C.c_int64
+        for name, args in {
+            "oracle_bf16_encode": [P, P, i64],
+            "oracle_bf16_decode": [P, P, i64],
+            "oracle_e4m3_encode": [P, P, i64],
+            "oracle_e4m3_decode": [P, P, i64],
+            "oracle_route": [i32, i32, i32, P, P, P, P],
+            "oracle_count": [i32, i32, i32, i32, i32, P, P, P, P, P, P],
+            "oracle_dispatch_bf16": [i32, i32, i32, i32, i32, P, P, P, P, P],
+            "oracle_dispatch_fp8": [i32, i32, i32, i32, i32, P, P, P, P, P, P],
+            "oracle_expert_synthetic": [i32, i32, i32, i32, P, P, P, P, P],
+            "oracle_combine": [i32, i32, i32, i32, i32, P, P, P, P, P],
+        }.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = None if name.startswith(("oracle_bf16", "oracle_e4m3")) else C.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"{what}: invalid argument")
+
+
+# ---- codecs -----------------------------------------------------------------
+
+def bf16_encode(f32: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(f32, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint16)
+    lib().oracle_bf16_encode(_p(a), _p(out), a.size)
+    return out
+
+
+def bf16_decode(bits: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(a.shape, dtype=np.float32)
+    lib().oracle_bf16_decode(_p(a), _p(out), a.size)
+    return out
+
+
+def e4m3_encode(f32: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(f32, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint8)
+    lib().oracle_e4m3_encode(_p(a), _p(out), a.size)
+    return out
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(a.shape, dtype=np.float32)
+    lib().oracle_e4m3_decode(_p(a), _p(out), a.size)
+    return out
+
+
+# ---- the path, step by step ---------------------------------------------------
+
+def route(logits: np.ndarray, k: int, with_double: bool = False):
+    """Top-k of each row of logits[T][E] and the renormalised softmax weights."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    w64 = np.empty((T, k), dtype=np.float64) if with_double else None
+    _check(lib().oracle_route(T, E, k, _p(lg), _p(idx), _p(w), _p(w64)), "oracle_route")
+    return (idx, w, w64) if with_double else (idx, w)
+
+
+def count(topk_idx: np.ndarray, E: int, R: int, Cap: int) -> dict:
+    """Histogram, exclusive scan, slots, per-rank row counts and drops."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = idx.shape
+    counts = np.empty(E, dtype=np.int32)
+    offsets = np.empty(E + 1, dtype=np.int32)
+    slot = np.empty((T, k), dtype=np.int32)
+    rank_counts = np.empty(R, dtype=np.int32)
+    dropped = np.zeros(1, dtype=np.int32)
+    _check(lib().oracle_count(T, E, k, R, Cap, _p(idx), _p(counts), _p(offsets), _p(slot),
+                              _p(rank_counts), _p(dropped)), "oracle_count")
+    return {"counts": counts, "offsets": offsets, "slot": slot,
+            "rank_counts": rank_counts, "dropped": int(dropped[0])}
+
+
+def dispatch_bf16(x: np.ndarray, topk_idx, slot, E: int, Cap: int, fill: int = 0):
+    xb = np.ascontiguousarray(x, dtype=np.uint16)
+    T, H = xb.shape
+    k = topk_idx.shape[1]
+    recv_x = np.full((E, Cap, H), fill, dtype=np.uint16)
+    recv_src = np.full((E, Cap), -1, dtype=np.int32)
+    _check(lib().oracle_dispatch_bf16(T, H, E, k, Cap, _p(xb), _p(np.ascontiguousarray(topk_idx, dtype=np.int32)),
+                                      _p(np.ascontiguousarray(slot, dtype=np.int32)), _p(recv_x), _p(recv_src)),
+           "oracle_dispatch_bf16")
+    return recv_x, recv_src
+
+
+def dispatch_fp8(x: np.ndarray, topk_idx, slot, E: int, Cap: int):
+    xb = np.ascontiguousarray(x, dtype=np.uint16)
+    T, H = xb.shape
+    k = topk_idx.shape[1]
+    recv_q = np.zeros((E, Cap, H), dtype=np.uint8)
+    recv_scale = np.zeros((E, Cap, H // 128), dtype=np.float32)
+    recv_src = np.full((E, Cap), -1, dtype=np.int32)
+    _check(lib().oracle_dispatch_fp8(T, H, E, k, Cap, _p(xb), _p(np.ascontiguousarray(topk_idx, dtype=np.int32)),
+                                     _p(np.ascontiguousarray(slot, dtype=np.int32)), _p(recv_q), _p(recv_scale),
+                                     _p(recv_src)), "oracle_dispatch_fp8")
+    return recv_q, recv_scale, recv_src
+
+
+def expert_synthetic(recv, recv_scale, counts, s):
+    """y = bf16(x * s_e) (bf16 recv) or bf16((q * scale) * s_e) (fp8 recv); valid rows only."""
+    E, Cap, H = recv.shape
+    fp8 = recv.dtype == np.uint8
+    y = np.zeros((E, Cap, H), dtype=np.uint16)
+    rs = np.ascontiguousarray(recv_scale, dtype=np.float32) if fp8 else None
+    _check(lib().oracle_expert_synthetic(H, E, Cap, int(fp8), _p(np.ascontiguousarray(recv)), _p(rs),
+                                         _p(np.ascontiguousarray(counts, dtype=np.int32)),
+                                         _p(np.ascontiguousarray(s, dtype=np.float32)), _p(y)),
+           "oracle_expert_synthetic")
+    return y
+
+
+def combine(y: np.ndarray, topk_idx, topk_w, slot, T: int):
+    E, Cap, H = y.shape
+    k = topk_idx.shape[1]
+    out = np.empty((T, H), dtype=np.uint16)
+    _check(lib().oracle_combine(T, H, E, k, Cap, _p(np.ascontiguousarray(y, dtype=np.uint16)),
+                                _p(np.ascontiguousarray(topk_idx, dtype=np.int32)),
+                                _p(np.ascontiguousarray(topk_w, dtype=np.float32)),
+                                _p(np.ascontiguousarray(slot, dtype=np.int32)), _p(out)), "oracle_combine")
+    return out
+
+
+def run_path(x, logits, s, k: int, R: int, Cap: int, fp8: bool) -> dict:
+    """Route -> count -> dispatch -> synthetic expert -> combine on one batch."""
+    T, E = logits.shape
+    idx, w = route(logits, k)
+    c = count(idx, E, R, Cap)
+    if fp8:
+        rq, rs, src = dispatch_fp8(x, idx, c["slot"], E, Cap)
+        y = expert_synthetic(rq, rs, c["counts"], s)
+        res = {"recv_q": rq, "recv_scale": rs}
+    else:
+        rx, src = dispatch_bf16(x, idx, c["slot"], E, Cap)
+        y = expert_synthetic(rx, None, c["counts"], s)
+        res = {"recv_x": rx}
+    out = combine(y, idx, w, c["slot"], T)
+    res.update(c)
+    res.update({"topk_idx": idx, "topk_w": w, "recv_src": src, "y": y, "out": out})
+    return res
+
+
+def micro_batches(T: int):
+    """[DBO §UBatchRunner]: the batch is split at its midpoint into two
+    micro-batches; a micro-batch with no tokens runs as an empty (dummy) batch.
+    Returns the token ranges [(0, T//2), (T//2, T)]."""
+    m = T // 2
+    return [(0, m), (m, T)]
+
+
+def run_dbo(x, logits, s, k: int, R: int, Cap: int, fp8: bool) -> dict:
+    """The two-micro-batch step: each half runs the whole path on its own
+    buffers; the output is the two halves' outputs in token order."""
+    T, E = logits.shape
+    H = x.shape[1]
+    outs, parts = [], []
+    for (a, b) in micro_batches(T):
+        if b == a:
+            parts.append(None)
+            outs.append(np.empty((0, H), dtype=np.uint16))
+            continue
+        r = run_path(x[a:b], logits[a:b], s, k, R, Cap, fp8)
+        parts.append(r)
+        outs.append(r["out"])
+    return {"out": np.concatenate(outs, axis=0), "parts": parts}
