@@ -1,0 +1,503 @@
+"""Benchmark of the MoE route / dispatch / combine path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload: DeepSeek-V3-shaped decode with fp8 dispatch (T=1024 tokens from 8
+virtual DP ranks, H=7168, E=256, k=8, R=8, C=128), seeded synthetic inputs
+resident in HBM. One step = moe_route -> moe_dispatch (fp8) ->
+moe_expert_synthetic -> moe_combine through the C ABI, with L2 flushed (a
+write and a read of 2x the L2 size) before every call; each call is bracketed
+by CUDA events on its stream and the flush is outside the brackets.
+
+  value        dispatch+combine tokens/s = tokens / (dispatch + combine time),
+               summed over replicas (N GPUs = N independent replicas, the
+               slowest rank's time).
+  ms_per_step  mean kernel time of the whole step (all four calls).
+  e2e          the same path through the public API with pinned host buffers:
+               H2D of x and logits, the four calls, D2H of out, per step.
+  roofline     the combine kernel (the larger of the two kernels the metric
+               names): algorithmic bytes / mean duration vs measured HBM peak.
+  cpu_baseline the CPU oracle, single-threaded, on a bounded sample.
+  dbo          the dual-batch-overlap step on the 8192-token prefill workload.
+
+--impl reference times the CPU oracle instead (the reference arm of this
+build), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+import workloads as W
+
+METRIC = "dispatch+combine tokens/s; achieved HBM GB/s vs GB300 peak (DeepSeek-V3 shape)"
+UNIT = "tokens/s"
+WORKLOAD = "dsv3_fp8"
+DTYPE = "e4m3+bf16 (fp32 arithmetic)"
+FALLBACK_HBM_GBS = 6800.0
+KERNELS_PER_STEP = 6          # route: top-k/tile, scan, slot; dispatch; expert; combine
+CPU_SAMPLE_TOKENS = 256       # the oracle's bounded sample: 2 of the 8 source ranks
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes per call (padding rows are never touched by the method)
+
+def bytes_route(w: W.Workload) -> int:
+    # logits in; topk_idx, topk_w, slot out; counts/offsets/rank_counts
+    return w.T * w.E * 4 + w.T * w.k * 12 + (2 * w.E + 1 + w.R + 1) * 4
+
+
+def bytes_dispatch(w: W.Workload, kept: int) -> int:
+    meta = w.T * w.k * 8 + kept * 4                       # topk_idx + slot in, recv_src out
+    if w.dtype == W.DTYPE_FP8_E4M3_B128:
+        return w.T * w.H * 2 + kept * (w.H + 4 * (w.H // 128)) + meta
+    return w.T * w.H * 2 + kept * w.H * 2 + meta
+
+
+def bytes_expert(w: W.Workload, kept: int) -> int:
+    if w.dtype == W.DTYPE_FP8_E4M3_B128:
+        return kept * (w.H + 4 * (w.H // 128)) + kept * w.H * 2
+    return kept * w.H * 2 * 2
+
+
+def bytes_combine(w: W.Workload, kept: int) -> int:
+    return kept * w.H * 2 + w.T * w.H * 2 + w.T * w.k * 12
+
+
+# ---------------------------------------------------------------------------
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            j = json.load(fh)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "combine_router_top_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+TRAFFIC_SOURCES = {"combine": ["moe_combine.cu", "moe_internal.cuh"],
+                   "dispatch": ["moe_dispatch.cu", "moe_internal.cuh"]}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha(TRAFFIC_SOURCES[kernel])
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == workload and f[2] == sha:
+            return int(float(f[3]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.rows = []
+        self.proc = None
+        self.err = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception as e:          # no nvidia-smi: report it, do not fail the bench
+            self.err = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"nvidia-smi unavailable: {self.err}"}
+        inside = [r for (t, r) in self.rows if t0 - 0.05 <= t <= t1 + 0.15]
+        note = "samples inside the timed region"
+        if not inside:
+            inside = [r for (_, r) in self.rows]
+            note = "timed region shorter than the sampling period: all samples of the run"
+        sm = [float(r[1]) for r in inside if len(r) > 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in inside if len(r) > 8 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside if len(r) > 8 for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def gpu_id_for_smi(torch, dev: int) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (reference arm and cpu_baseline)
+
+def oracle_sample(w: W.Workload, ntok: int):
+    """Seeded inputs of the first ntok tokens of workload w (same generator)."""
+    return W.make_x(w, 0, ntok), W.make_logits(w, 0, ntok), W.expert_scale(w)
+
+
+def time_oracle_step(O, x, lg, s, w: W.Workload) -> dict:
+    fp8 = w.dtype == W.DTYPE_FP8_E4M3_B128
+    t = {}
+    c0 = time.perf_counter()
+    idx, wt = O.route(lg, w.k)
+    c = O.count(idx, w.E, w.R, w.C)
+    c1 = time.perf_counter()
+    if fp8:
+        rq, rs, _ = O.dispatch_fp8(x, idx, c["slot"], w.E, w.C)
+    else:
+        rq, _ = O.dispatch_bf16(x, idx, c["slot"], w.E, w.C)
+        rs = None
+    c2 = time.perf_counter()
+    y = O.expert_synthetic(rq, rs, c["counts"], s)
+    c3 = time.perf_counter()
+    O.combine(y, idx, wt, c["slot"], x.shape[0])
+    c4 = time.perf_counter()
+    t.update(route=c1 - c0, dispatch=c2 - c1, expert=c3 - c2, combine=c4 - c3, step=c4 - c0)
+    return t
+
+
+def cpu_baseline(w: W.Workload, budget_s: float = 12.0, max_reps: int = 20) -> dict:
+    import oracle as O
+    x, lg, s = oracle_sample(w, CPU_SAMPLE_TOKENS)
+    O.lib()
+    time_oracle_step(O, x, lg, s, w)               # warm: library load, page faults
+    reps, tdc, tstep = 0, 0.0, 0.0
+    start = time.perf_counter()
+    while reps < max_reps and (reps < 2 or time.perf_counter() - start < budget_s):
+        t = time_oracle_step(O, x, lg, s, w)
+        tdc += t["dispatch"] + t["combine"]
+        tstep += t["step"]
+        reps += 1
+    return {"value": CPU_SAMPLE_TOKENS * reps / tdc, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {CPU_SAMPLE_TOKENS} of {w.T} tokens (2 of 8 source ranks), full E/H/k/C, "
+                      f"{reps} repetitions; value = tokens / (oracle dispatch + combine time); "
+                      f"whole oracle step {1e3 * tstep / reps:.1f} ms"}
+
+
+def config_of(w: W.Workload) -> dict:
+    return {"workload": f"{w.name}: T={w.T} tokens ({w.src_ranks} virtual DP ranks x {w.T // w.src_ranks}), "
+                        f"H={w.H}, E={w.E}, top_k={w.k}, R={w.R} virtual EP ranks, C={w.C}, "
+                        f"fp8 e4m3 block-128 dispatch, bf16 combine",
+            "T": w.T, "H": w.H, "E": w.E, "top_k": w.k, "R": w.R, "C": w.C,
+            "dispatch_dtype": "fp8_e4m3_b128" if w.dtype else "bf16",
+            "l2": "flushed before every call (write then read of 2x L2)", "parallelism": "replicas"}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    import oracle as O
+    w = W.WORKLOADS[WORKLOAD]
+    x, lg, s = oracle_sample(w, CPU_SAMPLE_TOKENS)
+    O.lib()
+    for _ in range(args.warmup):
+        time_oracle_step(O, x, lg, s, w)
+    tdc, tstep = 0.0, 0.0
+    for _ in range(args.steps):
+        t = time_oracle_step(O, x, lg, s, w)
+        tdc += t["dispatch"] + t["combine"]
+        tstep += t["step"]
+    value = CPU_SAMPLE_TOKENS * args.steps / tdc
+    sample = (f"each step: the oracle's whole path on the first {CPU_SAMPLE_TOKENS} of {w.T} tokens "
+              f"(full E/H/k/C); value = tokens / (dispatch + combine time)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tstep / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
+            "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# multi-GPU plumbing: N independent replicas, max over ranks
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank: int, world: int, local: int):
+    import torch
+    import combine_router_top_gb300 as M
+    from combine_router_top_gb300 import build as B
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if not os.path.exists(M.LIB_PATH):
+        B.build()
+    M.lib()
+    w = W.WORKLOADS[WORKLOAD]
+    fp8 = w.dtype == W.DTYPE_FP8_E4M3_B128
+    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
+    x_h, lg_h, s_h = W.make_x(w), W.make_logits(w), W.expert_scale(w)
+    x = torch.from_numpy(x_h.view(np.int16)).to(dev)
+    lg = torch.from_numpy(lg_h).to(dev)
+    s = torch.from_numpy(s_h).to(dev)
+    b = M.alloc_buffers(p, dev)
+    out = torch.empty((w.T, w.H), dtype=torch.int16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones_like(flush_w)
+    stream = torch.cuda.current_stream()
+
+    def flush():
+        flush_w.fill_(1)
+        flush_r.sum()
+
+    calls = [
+        ("route", lambda: M.moe_route(p, lg, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["slot"],
+                                      b["rank_counts"], b["dropped"], b["workspace"], stream)),
+        ("dispatch", lambda: M.moe_dispatch(p, x, b["topk_idx"], b["slot"], b["recv"], b.get("recv_scale"),
+                                            b["recv_src"], stream)),
+        ("expert", lambda: M.moe_expert_synthetic(p, b["recv"], b.get("recv_scale"), b["counts"], s, b["y"], stream)),
+        ("combine", lambda: M.moe_combine(p, b["y"], b["topk_idx"], b["topk_w"], b["slot"], out, stream)),
+    ]
+    for _ in range(max(args.warmup, 3)):
+        for _, fn in calls:
+            flush()
+            fn()
+    torch.cuda.synchronize()
+    kept = w.T * w.k - int(b["dropped"].item())
+
+    K = args.steps
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for n, _ in calls}
+    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    sampler.start()
+    time.sleep(0.4)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        for n, fn in calls:
+            flush()
+            ev[n][i][0].record(stream)
+            fn()
+            ev[n][i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world, dev)
+    sampler.stop()
+    ms = {n: statistics.fmean(a.elapsed_time(z) for a, z in ev[n]) for n, _ in calls}
+    step_ms = sum(ms.values())
+    dc_ms = reduce_max(ms["dispatch"] + ms["combine"], world, dev)
+    step_ms_max = reduce_max(step_ms, world, dev)
+    comb_ms = reduce_max(ms["combine"], world, dev)
+
+    # end to end through the public API: pinned host in, pinned host out
+    xp = torch.from_numpy(x_h.view(np.int16)).pin_memory()
+    lp = torch.from_numpy(lg_h).pin_memory()
+    op = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
+    x2, lg2, out2 = torch.empty_like(x), torch.empty_like(lg), torch.empty_like(out)
+
+    def e2e_step():
+        x2.copy_(xp, non_blocking=True)
+        lg2.copy_(lp, non_blocking=True)
+        M.run_path(p, x2, lg2, s, b, out2, stream)
+        op.copy_(out2, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    ke = max(5, min(K, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / ke, world, dev)
+    assert torch.equal(out2, out), "end-to-end output differs from the device-resident run"
+
+    peak, peak_kind = measured_peak()
+    cb = bytes_combine(w, kept)
+    per_call = {}
+    for n, f in [("route", lambda: bytes_route(w)), ("dispatch", lambda: bytes_dispatch(w, kept)),
+                 ("expert", lambda: bytes_expert(w, kept)), ("combine", lambda: cb)]:
+        by = f()
+        per_call[n] = {"us": 1e3 * ms[n], "algorithmic_bytes": by, "gbs": by / (ms[n] * 1e-3) / 1e9,
+                       "frac": by / (ms[n] * 1e-3) / 1e9 / peak}
+    line = None
+    if rank == 0:
+        achieved = cb / (comb_ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": world * w.T / (dc_ms * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": "synthetic", "config": config_of(w),
+            "roofline": {"kernel": "combine_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                         "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                         "traffic": ncu_traffic("combine", WORKLOAD),
+                         "algorithmic_bytes": cb},
+            "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": x.numel() * 2 + lg.numel() * 4, "d2h_bytes_per_step": out.numel() * 2,
+                    "ms_per_step": e2e_ms, "what": "H2D x+logits, route, dispatch, expert, combine, D2H out"},
+            "gpu_launches": KERNELS_PER_STEP * K,
+            "clocks": sampler.summary(t0, t1),
+            "calls": per_call,
+            "path_tokens_per_s": world * w.T / (step_ms_max * 1e-3),
+        }
+    return line, dev
+
+
+def run_dbo(args, dev) -> dict:
+    """Dual-batch-overlap step on the 8192-token prefill workload."""
+    import torch
+    import combine_router_top_gb300 as M
+    w = W.WORKLOADS["dbo"]
+    T0, T1 = w.T // 2, w.T - w.T // 2
+    pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C)
+    x = torch.from_numpy(W.make_x(w).view(np.int16)).to(dev)
+    lg = torch.from_numpy(W.make_logits(w)).to(dev)
+    s = torch.from_numpy(W.expert_scale(w)).to(dev)
+    bufs = [M.alloc_buffers(M.problem(T1, w.H, w.E, w.k, w.R, w.C), dev) for _ in range(2)]
+    out = torch.empty((w.T, w.H), dtype=torch.int16, device=dev)
+    comp, comm = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ctx = M.dbo_create()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+    flush_r = torch.ones_like(flush_w)
+    res = {"overlap_fraction": [], "step_ms": [], "dispatch_ub1_ms": [], "combine_ub0_ms": [], "serial_ms": []}
+    reps = 10
+    with torch.cuda.stream(comp):
+        for i in range(3 + reps):
+            flush_w.fill_(1)
+            flush_r.sum()
+            M.dbo_step(ctx, pf, x, lg, s, bufs, out, comp, comm, record_timing=True)
+            t = M.dbo_read_timing(ctx)
+            if i >= 3:
+                for key in ["overlap_fraction", "step_ms", "dispatch_ub1_ms", "combine_ub0_ms"]:
+                    res[key].append(t[key])
+        # the same work on one stream, for comparison
+        for i in range(3 + reps):
+            flush_w.fill_(1)
+            flush_r.sum()
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(comp)
+            for (lo, hi), bb in zip([(0, T0), (T0, w.T)], bufs):
+                p = M.problem(hi - lo, w.H, w.E, w.k, w.R, w.C)
+                M.run_path(p, x[lo:hi], lg[lo:hi], s, bb, out[lo:hi], comp)
+            z.record(comp)
+            z.synchronize()
+            if i >= 3:
+                res["serial_ms"].append(a.elapsed_time(z))
+    ctx.close()
+    med = {k: statistics.median(v) for k, v in res.items()}
+    kept1 = T1 * w.k - int(bufs[1]["dropped"].item())
+    kept0 = T0 * w.k - int(bufs[0]["dropped"].item())
+    wd = w.with_(T=T1)
+    wc = w.with_(T=T0)
+    return {"workload": f"dbo: T={w.T} split {T0}/{T1}, H={w.H}, E={w.E}, top_k={w.k}, R={w.R}, C={w.C}, bf16",
+            "overlap_fraction": med["overlap_fraction"], "dbo_step_ms": med["step_ms"],
+            "single_stream_ms": med["serial_ms"], "dispatch_ub1_ms": med["dispatch_ub1_ms"],
+            "combine_ub0_ms": med["combine_ub0_ms"],
+            "overlapped_pair_bytes": bytes_dispatch(wd, kept1) + bytes_combine(wc, kept0),
+            "reps": reps, "l2": "flushed before every step"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dbo", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    line, dev = run_ours(args, rank, world, local)
+    if rank == 0:
+        if world == 1 and not args.no_dbo:
+            line["dbo"] = run_dbo(args, dev)
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(W.WORKLOADS[WORKLOAD])
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

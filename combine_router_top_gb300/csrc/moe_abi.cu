@@ -1,0 +1,68 @@
+// moe_abi.cu -- status strings, argument validation and workspace sizing.
+// Host code only; nothing here touches the GPU except the cached SM count.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+int check_problem(const moe_problem *p, Dims *d) {
+    if (p == nullptr) return MOE_ERR_INVALID_ARG;
+    const long long T = p->num_tokens, H = p->hidden, E = p->num_experts, k = p->top_k;
+    const long long R = p->num_ranks, C = p->capacity;
+    if (T < 0 || T > kMaxTokens) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+    if (k < 1 || k > kMaxTopK || k > E) return MOE_ERR_INVALID_ARG;
+    if (R < 1 || R > E || E % R != 0) return MOE_ERR_INVALID_ARG;
+    if (C < 1 || C > kMaxCapacity) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H > kMaxHidden || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (p->dispatch_dtype != MOE_DTYPE_BF16 && p->dispatch_dtype != MOE_DTYPE_FP8_E4M3_B128)
+        return MOE_ERR_INVALID_ARG;
+    if (p->dispatch_dtype == MOE_DTYPE_FP8_E4M3_B128 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (p->max_blocks < 0) return MOE_ERR_INVALID_ARG;
+    if (T * k >= (1LL << 31) || E * C >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+    if (d) {
+        d->T = (int)T; d->H = (int)H; d->E = (int)E; d->k = (int)k;
+        d->R = (int)R; d->C = (int)C; d->dtype = p->dispatch_dtype; d->max_blocks = p->max_blocks;
+    }
+    return MOE_OK;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace moe
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: a size, pointer or alignment check failed";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: request outside what this build supports";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: the CUDA runtime reported an error";
+        case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK: a device-side consistency check failed";
+        default: return "unknown moe_status";
+    }
+}
+
+int moe_validate(const moe_problem *p) { return moe::check_problem(p, nullptr); }
+
+size_t moe_route_workspace_bytes(const moe_problem *p) {
+    moe::Dims d;
+    if (moe::check_problem(p, &d) != MOE_OK) return 0;
+    const size_t tiles = ((size_t)d.T + moe::kTileTokens - 1) / moe::kTileTokens;
+    size_t bytes = tiles * (size_t)d.E * sizeof(int32_t);
+    bytes = (bytes + 255) & ~(size_t)255;
+    return bytes < 256 ? 256 : bytes;
+}
+
+}  // extern "C"

@@ -1,0 +1,159 @@
+// moe_dbo.cu -- the dual-batch-overlap step on two CUDA streams of one GPU.
+//
+// [DBO §Introduction]: the batch is split into two micro-batches so that while
+// one computes, the other communicates. [DBO §UBatchRunner]: the split is at
+// the midpoint; a micro-batch with no tokens runs as a dummy (empty) batch.
+// [DBO §UBatchContext, §Interfaces]: the two micro-batch threads hand over at
+// yield points and a receive hook waits on the all-to-all. Here no host
+// threads are needed: the hand-over is a cudaEvent recorded on one stream and
+// waited on by the other, and the "all-to-all" of a micro-batch is its
+// dispatch (rows into the expert-major buffer) and its combine.
+//
+// Schedule (compute = caller's compute stream, comm = caller's comm stream):
+//   compute: route(0) route(1) dispatch(0) expert(0) [E0] combine(0) wait(D1) expert(1) combine(1)
+//   comm:    wait(entry) ........................ wait(E0) dispatch(1) [D1]
+// so dispatch of micro-batch 1 runs while micro-batch 0 combines. The two
+// overlapped kernels get a capped grid (grid-stride loops) so that both have
+// thread blocks resident at the same time.
+#include <new>
+
+#include "moe_internal.cuh"
+
+struct moe_dbo_ctx {
+    int device;
+    cudaEvent_t entry, expert0, dispatch1;                 // ordering only
+    cudaEvent_t t_start, t_d1_start, t_d1_end, t_c0_start, t_c0_end, t_end;   // timing
+    bool timed;
+};
+
+namespace {
+
+const char *byte_ptr(const void *p, size_t off) { return static_cast<const char *>(p) + off; }
+
+}  // namespace
+
+extern "C" int dbo_create(moe_dbo_ctx **out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    moe_dbo_ctx *c = new (std::nothrow) moe_dbo_ctx();
+    if (!c) return MOE_ERR_CUDA;
+    if (cudaGetDevice(&c->device) != cudaSuccess) { delete c; return MOE_ERR_CUDA; }
+    cudaEvent_t *sync_ev[] = {&c->entry, &c->expert0, &c->dispatch1};
+    cudaEvent_t *time_ev[] = {&c->t_start, &c->t_d1_start, &c->t_d1_end, &c->t_c0_start, &c->t_c0_end, &c->t_end};
+    bool ok = true;
+    for (auto e : sync_ev) ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    for (auto e : time_ev) ok = ok && cudaEventCreate(e) == cudaSuccess;
+    c->timed = false;
+    if (!ok) { dbo_destroy(c); return MOE_ERR_CUDA; }
+    *out = c;
+    return MOE_OK;
+}
+
+extern "C" void dbo_destroy(moe_dbo_ctx *c) {
+    if (!c) return;
+    cudaEvent_t evs[] = {c->entry, c->expert0, c->dispatch1, c->t_start, c->t_d1_start,
+                         c->t_d1_end, c->t_c0_start, c->t_c0_end, c->t_end};
+    for (auto e : evs)
+        if (e) cudaEventDestroy(e);
+    delete c;
+}
+
+extern "C" int dbo_step(moe_dbo_ctx *ctx, const moe_problem *full, const void *x, const float *logits,
+                        const float *s, const moe_ubatch_bufs *bufs, void *out, void *compute_stream,
+                        void *comm_stream, int record_timing) {
+    using namespace moe;
+    Dims d;
+    int rc = check_problem(full, &d);
+    if (rc != MOE_OK) return rc;
+    if (!ctx || !bufs || !s) return MOE_ERR_INVALID_ARG;
+    if (d.T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
+    if (compute_stream == comm_stream) return MOE_ERR_INVALID_ARG;
+
+    const int T0 = d.T / 2, T1 = d.T - T0;
+    moe_problem p[2] = {*full, *full};
+    p[0].num_tokens = T0;
+    p[1].num_tokens = T1;
+    // overlapped pair: at most two thread blocks per SM each
+    moe_problem p_overlap[2] = {p[0], p[1]};
+    const int cap = full->max_blocks > 0 ? full->max_blocks : 2 * sm_count();
+    p_overlap[0].max_blocks = cap;
+    p_overlap[1].max_blocks = cap;
+
+    const size_t xrow = (size_t)d.H * 2, lrow = (size_t)d.E * sizeof(float);
+    const void *x_ub[2] = {x, d.T ? byte_ptr(x, xrow * T0) : nullptr};
+    const float *l_ub[2] = {logits, d.T ? reinterpret_cast<const float *>(byte_ptr(logits, lrow * T0)) : nullptr};
+    void *o_ub[2] = {out, d.T ? static_cast<char *>(out) + xrow * T0 : nullptr};
+
+    cudaStream_t cs = as_stream(compute_stream), ms = as_stream(comm_stream);
+    const bool timed = record_timing != 0;
+#define MOE_TRY(call)                      \
+    do {                                   \
+        int _r = (call);                   \
+        if (_r != MOE_OK) return _r;       \
+    } while (0)
+#define MOE_CUDA(call)                                   \
+    do {                                                 \
+        if ((call) != cudaSuccess) return MOE_ERR_CUDA;  \
+    } while (0)
+
+    MOE_CUDA(cudaEventRecord(ctx->entry, cs));
+    MOE_CUDA(cudaStreamWaitEvent(ms, ctx->entry, 0));
+    if (timed) MOE_CUDA(cudaEventRecord(ctx->t_start, cs));
+
+    for (int u = 0; u < 2; ++u) {
+        const moe_ubatch_bufs &b = bufs[u];
+        MOE_TRY(moe_route(&p[u], l_ub[u], b.topk_idx, b.topk_w, b.counts, b.offsets, b.slot, b.rank_counts,
+                          b.dropped, b.workspace, b.workspace_bytes, compute_stream));
+    }
+    const moe_ubatch_bufs &b0 = bufs[0], &b1 = bufs[1];
+    MOE_TRY(moe_dispatch(&p[0], x_ub[0], b0.topk_idx, b0.slot, b0.recv, b0.recv_scale, b0.recv_src, compute_stream));
+    MOE_TRY(moe_expert_synthetic(&p[0], b0.recv, b0.recv_scale, b0.counts, s, b0.y, compute_stream));
+    MOE_CUDA(cudaEventRecord(ctx->expert0, cs));
+
+    // comm stream: dispatch of micro-batch 1
+    MOE_CUDA(cudaStreamWaitEvent(ms, ctx->expert0, 0));
+    if (timed) MOE_CUDA(cudaEventRecord(ctx->t_d1_start, ms));
+    MOE_TRY(moe_dispatch(&p_overlap[1], x_ub[1], b1.topk_idx, b1.slot, b1.recv, b1.recv_scale, b1.recv_src,
+                         comm_stream));
+    if (timed) MOE_CUDA(cudaEventRecord(ctx->t_d1_end, ms));
+    MOE_CUDA(cudaEventRecord(ctx->dispatch1, ms));
+
+    // compute stream: combine of micro-batch 0 overlaps the dispatch above
+    if (timed) MOE_CUDA(cudaEventRecord(ctx->t_c0_start, cs));
+    MOE_TRY(moe_combine(&p_overlap[0], b0.y, b0.topk_idx, b0.topk_w, b0.slot, o_ub[0], compute_stream));
+    if (timed) MOE_CUDA(cudaEventRecord(ctx->t_c0_end, cs));
+
+    MOE_CUDA(cudaStreamWaitEvent(cs, ctx->dispatch1, 0));
+    MOE_TRY(moe_expert_synthetic(&p[1], b1.recv, b1.recv_scale, b1.counts, s, b1.y, compute_stream));
+    MOE_TRY(moe_combine(&p[1], b1.y, b1.topk_idx, b1.topk_w, b1.slot, o_ub[1], compute_stream));
+    if (timed) MOE_CUDA(cudaEventRecord(ctx->t_end, cs));
+    ctx->timed = timed;
+#undef MOE_TRY
+#undef MOE_CUDA
+    return MOE_OK;
+}
+
+extern "C" int dbo_read_timing(moe_dbo_ctx *ctx, moe_dbo_timing *t) {
+    if (!ctx || !t) return MOE_ERR_INVALID_ARG;
+    if (!ctx->timed) return MOE_ERR_INVALID_ARG;
+    if (cudaEventSynchronize(ctx->t_end) != cudaSuccess) return MOE_ERR_CUDA;
+    float sd, ed, sc, ec, step;
+    if (cudaEventElapsedTime(&step, ctx->t_start, ctx->t_end) != cudaSuccess ||
+        cudaEventElapsedTime(&sd, ctx->t_start, ctx->t_d1_start) != cudaSuccess ||
+        cudaEventElapsedTime(&ed, ctx->t_start, ctx->t_d1_end) != cudaSuccess ||
+        cudaEventElapsedTime(&sc, ctx->t_start, ctx->t_c0_start) != cudaSuccess ||
+        cudaEventElapsedTime(&ec, ctx->t_start, ctx->t_c0_end) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const float dd = ed - sd, dc = ec - sc;
+    float ov = (ed < ec ? ed : ec) - (sd > sc ? sd : sc);
+    if (ov < 0.0f) ov = 0.0f;
+    const float shorter = dd < dc ? dd : dc;
+    float frac = shorter > 0.0f ? ov / shorter : 0.0f;
+    if (frac > 1.0f) frac = 1.0f;
+    t->step_ms = step;
+    t->dispatch_ub1_ms = dd;
+    t->combine_ub0_ms = dc;
+    t->overlap_ms = ov;
+    t->overlap_fraction = frac;
+    return MOE_OK;
+}

@@ -1,0 +1,87 @@
+// moe_internal.cuh -- internal helpers of libmoe_gb300 (not part of the ABI).
+//
+// Page abbreviations used in this library's comments:
+//   [PMC] "Efficient and portable mixture-of-experts communication" (Perplexity blog)
+//   [DBO] "Dual Batch Overlap" (vLLM design documentation)
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kTileTokens = 32;    // tokens per route tile: one 32-bit mask word per expert
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxHidden = 65536;
+constexpr int kMaxTokens = 1 << 24;
+constexpr int kMaxCapacity = 1 << 24;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// Validated sizes of one call.
+struct Dims {
+    int T, H, E, k, R, C, dtype, max_blocks;
+};
+
+// Host-side checks (moe_abi.cu).
+int check_problem(const moe_problem *p, Dims *d);
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+int sm_count();                         // SMs of the current device (cached)
+inline int launch_status(void) {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ---- device helpers -------------------------------------------------------
+
+// 16-byte load through the read-only path, not kept in L1 (each row is read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// bf16 pair in a 32-bit word -> two floats (exact: bf16 is the upper half of a binary32).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two floats -> bf16 pair, round to nearest even (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Two floats -> two e4m3 codes (round to nearest even, saturating to +-448), lo in the low byte.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+    __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+    return static_cast<uint32_t>(s);
+}
+
+// Total order on fp32 logits as unsigned keys: larger logit -> larger key,
+// -0.0 folded onto +0.0, NaN mapped to 1 (below every number), 0 reserved
+// for "no candidate".
+__device__ __forceinline__ uint32_t logit_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (f != f) return 1u;
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+}  // namespace moe

@@ -1,0 +1,226 @@
+// moe_route.cu -- steps 1 and 2 of the path: router top-k with renormalised
+// softmax weights, then the per-expert histogram, its exclusive scan and the
+// slot of every (token, choice) pair.
+//
+// [PMC §Introduction]: the router's probability distribution picks the top-K
+// experts and weights their outputs. [PMC §Dispatch]: a counting warp tallies
+// tokens per destination expert. [PMC §Portable kernels]: a fixed per-expert
+// bound lets every sender compute a unique destination address.
+//
+// Three launches, no atomics that decide an order:
+//   K1 route_topk_tile: one CTA per tile of 32 tokens, one warp per token.
+//      Top-k by k rounds of a warp arg-max (redux.sync max on an order-
+//      preserving 32-bit key, ballot for the lowest tied lane). Weights by
+//      expf and one IEEE division. Each chosen expert sets the token's bit in
+//      a per-expert 32-bit shared-memory mask; a pair's rank within the tile is
+//      the popcount of the lower bits, the tile's count per expert the popcount.
+//   K2 route_scan: one CTA. Exclusive scan over tiles per expert (tile bases,
+//      in place in the workspace), totals, offsets, rank counts, drops.
+//   K3 route_slot: slot = tile base + rank in tile, or -1 beyond capacity.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+// Lane l of a token's warp owns experts [l*V, l*V + V) (clipped to E).
+template <int V>
+__global__ void __launch_bounds__(1024, 1)
+route_topk_tile_kernel(const float *__restrict__ logits, int T, int E, int k,
+                       int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+                       int32_t *__restrict__ slot_rank, int32_t *__restrict__ tile_counts) {
+    __shared__ uint32_t mask[kMaxExperts];
+    const int lane = threadIdx.x & 31;
+    const int wt = threadIdx.x >> 5;                 // token within the tile
+    const int tile = blockIdx.x;
+    const int t = tile * kTileTokens + wt;
+    const bool active = t < T;                       // warp-uniform
+    for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0u;
+    __syncthreads();
+
+    int my_e = 0;
+    if (active) {
+        const int e0 = lane * V;
+        const float *row = logits + (size_t)t * E;
+        uint32_t key[V];
+        if ((V % 4) == 0 && (E % 4) == 0 && e0 + V <= E) {
+#pragma unroll
+            for (int i = 0; i < V; i += 4) {
+                const float4 f = __ldg(reinterpret_cast<const float4 *>(row + e0 + i));
+                key[i] = logit_key(f.x);
+                key[i + 1] = logit_key(f.y);
+                key[i + 2] = logit_key(f.z);
+                key[i + 3] = logit_key(f.w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) key[i] = (e0 + i < E) ? logit_key(__ldg(row + e0 + i)) : 0u;
+        }
+
+        uint32_t my_key = 0, top_key = 0;
+        for (int j = 0; j < k; ++j) {
+            // the lane's best remaining candidate (lowest index among equals)
+            uint32_t best = 0;
+            int bi = 0;
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                if (key[i] > best) { best = key[i]; bi = i; }
+            const uint32_t m = __reduce_max_sync(kFull, best);
+            // lanes own ascending index ranges: the lowest tied lane holds the lowest index
+            const int wl = __ffs(__ballot_sync(kFull, best == m)) - 1;
+            const int e = __shfl_sync(kFull, e0 + bi, wl);
+            if (lane == wl) {
+#pragma unroll
+                for (int i = 0; i < V; ++i)
+                    if (i == bi) key[i] = 0u;
+            }
+            if (lane == j) { my_key = m; my_e = e; }
+            if (j == 0) top_key = m;
+        }
+
+        // w_j = exp(l_j - l_0) / sum_{i<k} exp(l_i - l_0)
+        float ex = 0.0f;
+        if (lane < k) ex = expf(key_logit(my_key) - key_logit(top_key));
+        float sum = ex;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+        if (lane < k) {
+            topk_idx[(size_t)t * k + lane] = my_e;
+            topk_w[(size_t)t * k + lane] = __fdiv_rn(ex, sum);
+            atomicOr(&mask[my_e], 1u << wt);
+        }
+    }
+    __syncthreads();
+    if (active && lane < k)
+        slot_rank[(size_t)t * k + lane] = __popc(mask[my_e] & ((1u << wt) - 1u));
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        tile_counts[(size_t)tile * E + e] = __popc(mask[e]);
+}
+
+__global__ void __launch_bounds__(1024, 1)
+route_scan_kernel(int n_tiles, int E, int R, int C, int32_t *__restrict__ wc,
+                  int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                  int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped) {
+    __shared__ int32_t part[1024];
+    __shared__ int32_t tot[kMaxExperts];
+    __shared__ int32_t racc[kMaxExperts];
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t dacc;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = (1024 / E) > 0 ? (1024 / E) : 1;   // groups of E threads split the tiles
+    const int g = tid / E, e = tid % E;
+    const bool on = g < G;
+    const int per = (n_tiles + G - 1) / G;
+    const int b0 = min(n_tiles, g * per), b1 = min(n_tiles, b0 + per);
+
+    if (on) {
+        int s = 0;
+#pragma unroll 8
+        for (int b = b0; b < b1; ++b) s += wc[(size_t)b * E + e];
+        part[tid] = s;
+    }
+    for (int i = tid; i < E; i += blockDim.x) racc[i] = 0;
+    if (tid == 0) dacc = 0;
+    __syncthreads();
+    if (on) {
+        int run = 0;
+        for (int gg = 0; gg < g; ++gg) run += part[gg * E + e];
+        for (int b = b0; b < b1; ++b) {
+            const int c = wc[(size_t)b * E + e];
+            wc[(size_t)b * E + e] = run;
+            run += c;
+        }
+        if (g == G - 1) tot[e] = run;
+    }
+    __syncthreads();
+
+    // offsets = exclusive scan of the totals over experts
+    const int v = tid < E ? tot[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int ws = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(kFull, ws, o);
+            if (lane >= o) ws += n;
+        }
+        warp_sums[lane] = ws;
+    }
+    __syncthreads();
+    const int excl = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (tid < E) {
+        counts[tid] = v;
+        offsets[tid] = excl;
+        if (tid == E - 1) offsets[E] = excl + v;
+        atomicAdd(&racc[tid / (E / R)], v < C ? v : C);          // integer sums: order-free
+        if (v > C) atomicAdd(&dacc, v - C);
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += blockDim.x) rank_counts[r] = racc[r];
+    if (tid == 0) *dropped = dacc;
+}
+
+__global__ void route_slot_kernel(int n_pairs, int k, int E, int C,
+                                  const int32_t *__restrict__ topk_idx,
+                                  const int32_t *__restrict__ tile_base,
+                                  int32_t *__restrict__ slot) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_pairs) return;
+    const int tile = (i / k) / kTileTokens;
+    const int s = tile_base[(size_t)tile * E + topk_idx[i]] + slot[i];
+    slot[i] = s < C ? s : -1;
+}
+
+template <int V>
+void launch_topk(int n_tiles, cudaStream_t st, const float *logits, const Dims &d, int32_t *idx,
+                 float *w, int32_t *slot, int32_t *wc) {
+    route_topk_tile_kernel<V><<<n_tiles, 1024, 0, st>>>(logits, d.T, d.E, d.k, idx, w, slot, wc);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *topk_idx, float *topk_w,
+                         int32_t *counts, int32_t *offsets, int32_t *slot, int32_t *rank_counts,
+                         int32_t *dropped, void *workspace, size_t workspace_bytes, void *stream) {
+    using namespace moe;
+    Dims d;
+    int rc = check_problem(p, &d);
+    if (rc != MOE_OK) return rc;
+    if (!counts || !offsets || !rank_counts || !dropped || !workspace) return MOE_ERR_INVALID_ARG;
+    if (d.T > 0 && (!logits || !topk_idx || !topk_w || !slot)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < moe_route_workspace_bytes(p)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16) || !aligned(counts, 4) || !aligned(offsets, 4) ||
+        !aligned(rank_counts, 4) || !aligned(dropped, 4))
+        return MOE_ERR_INVALID_ARG;
+    // 16-byte vector loads of logit rows are used only when E % 4 == 0
+    const size_t logit_align = (d.E % 4 == 0) ? 16 : 4;
+    if (d.T > 0 && (!aligned(logits, logit_align) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+                    !aligned(slot, 4)))
+        return MOE_ERR_INVALID_ARG;
+
+    cudaStream_t st = as_stream(stream);
+    int32_t *wc = static_cast<int32_t *>(workspace);
+    const int n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
+    if (n_tiles > 0) {
+        const int per_lane = (d.E + 31) / 32;
+        if (per_lane <= 1) launch_topk<1>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else if (per_lane <= 2) launch_topk<2>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else if (per_lane <= 4) launch_topk<4>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else if (per_lane <= 8) launch_topk<8>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else if (per_lane <= 16) launch_topk<16>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else launch_topk<32>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+    }
+    route_scan_kernel<<<1, 1024, 0, st>>>(n_tiles, d.E, d.R, d.C, wc, counts, offsets, rank_counts, dropped);
+    if (d.T > 0) {
+        const int n_pairs = d.T * d.k;
+        route_slot_kernel<<<(n_pairs + 255) / 256, 256, 0, st>>>(n_pairs, d.k, d.E, d.C, topk_idx, wc, slot);
+    }
+    return launch_status();
+}

@@ -1,0 +1,225 @@
+/*
+ * moe.h -- C ABI of libmoe_gb300: the Mixture-of-Experts token path on one
+ * NVIDIA GB300 (sm_103a): router top-k, per-expert count and scan, dispatch
+ * into expert-major capacity-padded buffers, and top-k weighted combine, plus
+ * a two-stream dual-batch-overlap step.
+ *
+ * Pages the operations follow (title, section):
+ *   [PMC] "Efficient and portable mixture-of-experts communication"
+ *         (Perplexity, 2025-04-02), read in its Indonesian translation
+ *         "Komunikasi mixture-of-experts yang efisien dan portabel".
+ *   [DBO] "Dual Batch Overlap" (vLLM design documentation).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every buffer pointer is a DEVICE pointer (cudaMalloc / PyTorch CUDA
+ *   tensor) on the current device, allocated and owned by the caller, unless a
+ *   parameter says "host". The library never allocates, frees or synchronises
+ *   inside these calls, which matches [PMC §Portable kernels] (buffers are
+ *   sized once and reused across layers) and [PMC §Combine] (the result goes to
+ *   an externally allocated tensor).
+ * Streams.  `stream` is a cudaStream_t passed as void*; NULL is the legacy
+ *   default stream. Work is enqueued asynchronously on it, in argument order.
+ * Errors.  Arguments are checked on the host before anything is launched. A
+ *   failing call returns a negative moe_status and launches nothing. A launch
+ *   failure reported by the CUDA runtime returns MOE_ERR_CUDA. No call aborts.
+ * Sizes.  T = num_tokens, H = hidden, E = num_experts, k = top_k,
+ *   R = num_ranks, C = capacity, Er = E/R experts per virtual rank.
+ *   Limits: 0 <= T <= 2^24, 8 <= H <= 65536 with H % 8 == 0 (H % 128 == 0 for
+ *   fp8), 1 <= E <= 1024, 1 <= k <= min(E, 16), 1 <= R <= E with E % R == 0,
+ *   1 <= C <= 2^24, and T*k, E*C below 2^31. T == 0 is a valid empty batch:
+ *   the call returns MOE_OK after writing the all-zero counts it implies.
+ * Alignment.  Row buffers (x, recv, recv_scale, y, out) must be 16-byte
+ *   aligned, logits too when E % 4 == 0 (4-byte otherwise); int32/float
+ *   arrays 4-byte aligned; the route workspace 16-byte aligned.
+ * Layouts (row-major, C order):
+ *   logits[T][E] f32; topk_idx[T][k] i32; topk_w[T][k] f32; slot[T][k] i32;
+ *   x[T][H] bf16; recv[E][C][H] bf16 or e4m3; recv_scale[E][C][H/128] f32;
+ *   recv_src[E][C] i32; y[E][C][H] bf16; out[T][H] bf16.
+ *   Expert e belongs to virtual expert-parallel rank e / Er and owns rows
+ *   [e*C, (e+1)*C) of recv / y, so [R][Er][C][H] and [E][C][H] are the same
+ *   memory: the receive buffer of [PMC §Portable kernels] for every rank at
+ *   once, in this one GPU's HBM.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,   /* a size, pointer or alignment check failed       */
+    MOE_ERR_UNSUPPORTED = -2,   /* valid request outside what this build supports  */
+    MOE_ERR_CUDA = -3,          /* the CUDA runtime reported an error               */
+    MOE_ERR_DEVICE_CHECK = -4   /* a device-side consistency check failed           */
+} moe_status;
+
+typedef enum moe_dispatch_dtype {
+    MOE_DTYPE_BF16 = 0,         /* rows are copied as bf16                          */
+    MOE_DTYPE_FP8_E4M3_B128 = 1 /* rows are quantised to e4m3, one f32 scale / 128  */
+} moe_dispatch_dtype;
+
+/* The problem statement: hidden states of T tokens, their router logits over
+ * E experts, top-k, R virtual expert-parallel ranks and a per-expert capacity
+ * C ([PMC §Portable kernels]: the maximum number of tokens is fixed, which
+ * bounds what each expert can receive). */
+typedef struct moe_problem {
+    int32_t num_tokens;      /* T */
+    int32_t hidden;          /* H */
+    int32_t num_experts;     /* E */
+    int32_t top_k;           /* k */
+    int32_t num_ranks;       /* R */
+    int32_t capacity;        /* C */
+    int32_t dispatch_dtype;  /* moe_dispatch_dtype */
+    int32_t max_blocks;      /* 0: library default grid; > 0: at most this many
+                                thread blocks for dispatch / expert / combine, so
+                                that kernels on another stream stay co-resident */
+} moe_problem;
+
+/* Human-readable name of a moe_status value. Never NULL; static storage. */
+const char *moe_status_string(int status);
+
+/* Host-only validation of a problem (no CUDA call). Returns MOE_OK or
+ * MOE_ERR_INVALID_ARG. */
+int moe_validate(const moe_problem *p);
+
+/* Bytes of device workspace moe_route needs for this problem (host-only, no
+ * CUDA call); 0 if the problem is invalid. The workspace holds one 32-bit
+ * count per (tile of 32 tokens, expert). Its contents need no initialisation. */
+size_t moe_route_workspace_bytes(const moe_problem *p);
+
+/* Step 1 and 2: router top-k with renormalised softmax weights, then the
+ * per-expert histogram, its exclusive scan and every pair's slot.
+ *
+ *  [PMC §Introduction]: the router gives a probability distribution over the
+ *  experts; the top-K experts are chosen and the output is their weighted
+ *  average with weights from that distribution. Here, per token t:
+ *    topk_idx[t][0..k-1]: the k largest logits, largest first; equal logits go
+ *                         to the lower expert index (-0.0 equals +0.0);
+ *    topk_w[t][j] = exp(l_j - l_0) / sum_{i<k} exp(l_i - l_0)  (fp32).
+ *  [PMC §Dispatch]: tokens are counted per destination expert; [PMC §Portable
+ *  kernels]: a fixed per-expert bound gives every row a unique address with no
+ *  synchronisation between senders. Here:
+ *    counts[e]      = number of pairs (t, j) with topk_idx[t][j] == e;
+ *    offsets[e]     = sum_{e' < e} counts[e'], offsets[E] = T*k  (E+1 entries);
+ *    slot[t][j]     = number of tokens t' < t that chose the same expert, or -1
+ *                     when that number is >= C (the pair is dropped);
+ *    rank_counts[r] = sum over experts e of rank r of min(counts[e], C);
+ *    dropped[0]     = sum_e max(0, counts[e] - C).
+ *  Capacity overflow is not an error: it shows in dropped and slot == -1.
+ *  Results are deterministic and independent of the launch configuration.
+ *  NaN logits give unspecified (but in-range) indices.
+ *  workspace: device scratch of at least moe_route_workspace_bytes(p) bytes,
+ *  16-byte aligned, not shared with a concurrent call. */
+int moe_route(const moe_problem *p, const float *logits,
+              int32_t *topk_idx, float *topk_w,
+              int32_t *counts, int32_t *offsets, int32_t *slot,
+              int32_t *rank_counts, int32_t *dropped,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Step 3: dispatch. [PMC §Dispatch]: rows are placed into one tensor for the
+ * downstream grouped GEMM, all tokens of one expert grouped together whatever
+ * their source, and each row's origin is stored so that combine can send it
+ * back. For every pair with slot[t][j] >= 0 and e = topk_idx[t][j]:
+ *   MOE_DTYPE_BF16:          recv[e][slot][:] = x[t][:] (bit copy);
+ *   MOE_DTYPE_FP8_E4M3_B128: per block b of 128 elements of x[t]:
+ *       scale = amax_b / 448 (fp32 division; 1.0 if amax_b == 0),
+ *       recv[e][slot][i] = e4m3(x[t][i] / scale) (round to nearest even,
+ *       saturating to +-448), recv_scale[e][slot][b] = scale
+ *     ([PMC §Dispatch]: tokens travel with their block scaling factors);
+ *   recv_src[e][slot] = t.
+ * Rows at slots >= min(counts[e], C) are not written. recv_scale must be NULL
+ * for bf16 and non-NULL for fp8. topk_idx and slot are moe_route's outputs. */
+int moe_dispatch(const moe_problem *p, const void *x,
+                 const int32_t *topk_idx, const int32_t *slot,
+                 void *recv, float *recv_scale, int32_t *recv_src, void *stream);
+
+/* Stand-in for the grouped expert GEMM that [PMC §Dispatch] feeds: on rows
+ * r < min(counts[e], C) of every expert,
+ *   bf16 recv:  y[e][r] = bf16(x * s[e]);
+ *   fp8 recv:   y[e][r] = bf16((e4m3_value * recv_scale) * s[e]);
+ * fp32 products, bf16 round to nearest even. Other rows of y are not written.
+ * s: device float[E]. recv_scale: NULL for bf16, the dispatch scales for fp8. */
+int moe_expert_synthetic(const moe_problem *p, const void *recv, const float *recv_scale,
+                         const int32_t *counts, const float *s, void *y, void *stream);
+
+/* Step 4: combine. [PMC §Combine]: the expert outputs are read back through
+ * the routing table and summed with the router weights into an externally
+ * allocated tensor:
+ *   out[t] = bf16( sum_j topk_w[t][j] * y[topk_idx[t][j]][slot[t][j]] )
+ * accumulated in fp32, one fused multiply-add per j in ascending j, from 0;
+ * pairs with slot == -1 are skipped (no renormalisation). */
+int moe_combine(const moe_problem *p, const void *y,
+                const int32_t *topk_idx, const float *topk_w, const int32_t *slot,
+                void *out, void *stream);
+
+/* ---- Dual batch overlap ------------------------------------------------- */
+
+/* Buffers of one micro-batch, each sized for its token count (see dbo_step). */
+typedef struct moe_ubatch_bufs {
+    int32_t *topk_idx;     /* [Tu][k]   */
+    float *topk_w;         /* [Tu][k]   */
+    int32_t *counts;       /* [E]       */
+    int32_t *offsets;      /* [E+1]     */
+    int32_t *slot;         /* [Tu][k]   */
+    int32_t *rank_counts;  /* [R]       */
+    int32_t *dropped;      /* [1]       */
+    void *recv;            /* [E][C][H] bf16 or e4m3 */
+    float *recv_scale;     /* [E][C][H/128] for fp8, else NULL */
+    int32_t *recv_src;     /* [E][C]    */
+    void *y;               /* [E][C][H] bf16 */
+    void *workspace;       /* route workspace for Tu tokens */
+    size_t workspace_bytes;
+} moe_ubatch_bufs;
+
+/* Event timing of the overlapped pair of the last dbo_step that recorded it
+ * (milliseconds, from CUDA events). overlap_fraction = time both kernels were
+ * running / the shorter kernel's duration, in [0, 1]. */
+typedef struct moe_dbo_timing {
+    float step_ms;              /* first to last event of the step            */
+    float dispatch_ub1_ms;      /* dispatch of micro-batch 1 (comm stream)    */
+    float combine_ub0_ms;       /* combine of micro-batch 0 (compute stream)  */
+    float overlap_ms;           /* time both were running                     */
+    float overlap_fraction;
+} moe_dbo_timing;
+
+typedef struct moe_dbo_ctx moe_dbo_ctx;   /* owns CUDA events only */
+
+/* Creates a context on the current device (cudaEventCreate only). */
+int dbo_create(moe_dbo_ctx **ctx);
+/* Destroys a context and its events. NULL is a no-op. */
+void dbo_destroy(moe_dbo_ctx *ctx);
+
+/* One dual-batch-overlap step over T = full->num_tokens tokens.
+ * [DBO §UBatchRunner]: the batch is split at its midpoint; micro-batch 0 is
+ * tokens [0, T/2) and micro-batch 1 is [T/2, T) (floor); a micro-batch with
+ * no tokens is run as an empty batch. [DBO §Introduction]: while one
+ * micro-batch computes, the other communicates. Here the two micro-batches
+ * run the whole path on their own buffers (bufs[0], bufs[1]; recv_src and
+ * slot hold micro-batch-local token indices) and the dispatch of micro-batch 1
+ * on `comm` overlaps the combine of micro-batch 0 on `compute`:
+ *   compute: route(0) route(1) dispatch(0) expert(0) | combine(0) | wait(D1) expert(1) combine(1)
+ *   comm:                      wait(route(1), expert(0)) dispatch(1) -> D1
+ * `comm` first waits for the work already on `compute`; at return all work of
+ * the step is ordered before later work on `compute`. out[T][H] receives both
+ * micro-batches' rows in token order and equals two single-shot runs.
+ * record_timing != 0 records events for dbo_read_timing. */
+int dbo_step(moe_dbo_ctx *ctx, const moe_problem *full,
+             const void *x, const float *logits, const float *s,
+             const moe_ubatch_bufs *bufs /* [2] */, void *out,
+             void *compute_stream, void *comm_stream, int record_timing);
+
+/* Waits for the events of the last step that recorded timing (host
+ * synchronisation: call it outside a timed or captured region) and fills *t. */
+int dbo_read_timing(moe_dbo_ctx *ctx, moe_dbo_timing *t /* host */);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -122,7 +122,8 @@ def dispatch_bf16(x: np.ndarray, topk_idx, slot, E: int, Cap: int, fill: int = 0
     xb = np.ascontiguousarray(x, dtype=np.uint16)
     T, H = xb.shape
     k = topk_idx.shape[1]
-    recv_x = np.full((E, Cap, H), fill, dtype=np.uint16)
+    # untouched pages of np.zeros stay unallocated: only written rows cost memory
+    recv_x = np.zeros((E, Cap, H), dtype=np.uint16) if fill == 0 else np.full((E, Cap, H), fill, dtype=np.uint16)
     recv_src = np.full((E, Cap), -1, dtype=np.int32)
     _check(lib().oracle_dispatch_bf16(T, H, E, k, Cap, _p(xb), _p(np.ascontiguousarray(topk_idx, dtype=np.int32)),
                                       _p(np.ascontiguousarray(slot, dtype=np.int32)), _p(recv_x), _p(recv_src)),

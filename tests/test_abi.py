@@ -1,0 +1,130 @@
+"""The C-ABI library loads, exports every entry point include/moe.h declares,
+and validates arguments on the host (no GPU needed: every call here returns
+before anything is launched)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from combine_router_top_gb300 import build as B
+    B.build()
+    import combine_router_top_gb300 as M
+    return M
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*([a-z_][a-z_0-9]*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_path(moe):
+    names = declared_functions()
+    for n in ["moe_route", "moe_dispatch", "moe_combine", "moe_expert_synthetic", "dbo_step", "dbo_create",
+              "dbo_destroy", "dbo_read_timing", "moe_status_string", "moe_validate", "moe_route_workspace_bytes"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r" T (\S+)", out))
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(moe.lib(), n)
+    assert set(moe.EXPORTS) == set(declared_functions())
+
+
+def test_library_does_not_export_cuda_runtime(moe):
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    assert not re.search(r" T cuda", out)
+
+
+def test_status_strings(moe):
+    for s in [0, -1, -2, -3, -4]:
+        assert moe.moe_status_string(s).startswith("MOE_")
+    assert moe.moe_status_string(12345) == "unknown moe_status"
+
+
+GOOD = dict(T=1024, H=7168, E=256, k=8, R=8, Cap=128, dtype=1)
+
+
+def mk(moe, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return moe.problem(a["T"], a["H"], a["E"], a["k"], a["R"], a["Cap"], a["dtype"], a.get("mb", 0))
+
+
+@pytest.mark.parametrize("bad", [
+    dict(k=0), dict(k=17), dict(E=4, k=5, R=4), dict(E=1025, R=1), dict(E=0), dict(R=0), dict(R=3),
+    dict(Cap=0), dict(T=-1), dict(H=12, dtype=0), dict(H=0), dict(H=7168 + 8), dict(dtype=2),
+    dict(H=65536 + 8, dtype=0), dict(mb=-1), dict(T=(1 << 24) + 1),
+])
+def test_validate_rejects(moe, bad):
+    assert moe.moe_validate(mk(moe, **bad)) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_route_workspace_bytes(mk(moe, **bad)) == 0
+
+
+def test_validate_accepts_workloads(moe):
+    import workloads as W
+    for w in W.WORKLOADS.values():
+        p = moe.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
+        assert moe.moe_validate(p) == moe.MOE_OK
+    assert moe.moe_validate(mk(moe, T=0)) == moe.MOE_OK
+    assert moe.moe_validate(mk(moe, H=8, dtype=0, E=1, k=1, R=1)) == moe.MOE_OK
+
+
+def test_route_workspace_bytes(moe):
+    p = mk(moe)        # 1024 tokens -> 32 tiles of 32, 256 experts, int32
+    assert moe.moe_route_workspace_bytes(p) == 32 * 256 * 4
+    assert moe.moe_route_workspace_bytes(mk(moe, T=0)) == 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=33, E=8, R=2)) % 256 == 0
+
+
+def test_calls_reject_bad_arguments_before_any_launch(moe):
+    L = moe.lib()
+    p = mk(moe)
+    fake = C.c_void_p(1 << 40)           # never dereferenced: checks fail first
+    # null problem
+    assert L.moe_route(None, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    # workspace too small
+    assert L.moe_route(C.byref(p), fake, fake, fake, fake, fake, fake, fake, fake, fake, 16, None) == moe.MOE_ERR_INVALID_ARG
+    # misaligned logits
+    odd = C.c_void_p((1 << 40) + 4)
+    assert L.moe_route(C.byref(p), odd, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    # fp8 dispatch needs recv_scale; bf16 must not have one
+    assert L.moe_dispatch(C.byref(p), fake, fake, fake, fake, None, fake, None) == moe.MOE_ERR_INVALID_ARG
+    pb = mk(moe, dtype=0)
+    assert L.moe_dispatch(C.byref(pb), fake, fake, fake, fake, fake, fake, None) == moe.MOE_ERR_INVALID_ARG
+    # misaligned row buffer
+    assert L.moe_combine(C.byref(p), odd, fake, fake, fake, fake, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(C.byref(p), fake, fake, fake, fake, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_expert_synthetic(C.byref(p), fake, None, fake, fake, fake, None) == moe.MOE_ERR_INVALID_ARG
+    # dbo: null context, same stream for both roles
+    arr = (moe.moe_ubatch_bufs * 2)()
+    assert L.dbo_step(None, C.byref(p), fake, fake, fake, arr, fake, None, None, 0) == moe.MOE_ERR_INVALID_ARG
+    assert L.dbo_read_timing(None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_calls_are_noops_without_gpu(moe):
+    """T == 0: dispatch and combine return MOE_OK without launching anything."""
+    L = moe.lib()
+    p = mk(moe, T=0)
+    fake = C.c_void_p(1 << 40)
+    assert L.moe_dispatch(C.byref(p), None, None, None, None, fake, None, None) == moe.MOE_OK
+    assert L.moe_combine(C.byref(p), None, None, None, None, None, None) == moe.MOE_OK
+
+
+def test_binding_refuses_cpu_tensors(moe):
+    import torch
+    p = mk(moe, T=4, H=256, E=8, k=2, R=2, Cap=4, dtype=0)
+    t = torch.zeros(16, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        moe.moe_combine(p, t, t, t, t, t)

@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle
+on the same seeded inputs.
+
+Bars: indices, counts, offsets, slots, rank counts, drops and dispatched
+buffers (bf16 rows, e4m3 codes, fp32 scales, recv_src) bit-exact; routing
+weights within 1e-6 relative; combine output within 1 bf16 ulp of the oracle's
+chained result, and bit-exact when the CUDA combine is given the oracle's own
+expert output and routing (both accumulate with one fp32 FMA per expert in
+selection order).
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    from combine_router_top_gb300 import build as B
+    B.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def run_both(w: W.Workload, x=None, logits=None, s=None, max_blocks=0, isolate=True):
+    from gpu_path import run_stages
+    x = W.make_x(w) if x is None else x
+    logits = W.make_logits(w) if logits is None else logits
+    s = W.expert_scale(w) if s is None else s
+    fp8 = w.dtype == W.DTYPE_FP8_E4M3_B128
+    o = O.run_path(x, logits, s, w.k, w.R, w.C, fp8)
+    g = run_stages(x, logits, s, w.k, w.R, w.C, fp8, max_blocks=max_blocks, oracle_inputs=o if isolate else None)
+    return g, o
+
+
+@pytest.mark.parametrize("name", ["tiny", "v2lite", "mixtral_skew", "dsv3_fp8"])
+def test_workload_parity(name):
+    from gpu_path import compare
+    w = W.WORKLOADS[name]
+    g, o = run_both(w)
+    compare(g, o, w.C, w.dtype == W.DTYPE_FP8_E4M3_B128)
+
+
+@pytest.mark.parametrize("max_blocks", [1, 7, 152, 1000])
+def test_results_do_not_depend_on_the_grid(max_blocks):
+    """Capped grids (grid-stride loops, as the overlapped kernels of the
+    dual-batch step use) give bit-identical results."""
+    from gpu_path import run_stages
+    w = W.WORKLOADS["dsv3_fp8"].with_(T=300)
+    x, lg, s = W.make_x(w), W.make_logits(w), W.expert_scale(w)
+    a = run_stages(x, lg, s, w.k, w.R, w.C, True)
+    b = run_stages(x, lg, s, w.k, w.R, w.C, True, max_blocks=max_blocks)
+    for key in a:
+        assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
+
+
+EDGE = {
+    # ragged token counts: partial 32-token tiles, partial waves
+    "T1": W.WORKLOADS["v2lite"].with_(T=1),
+    "T77": W.WORKLOADS["v2lite"].with_(T=77),
+    "T33_fp8": W.WORKLOADS["dsv3_fp8"].with_(T=33),
+    # capacity overflow: pairs dropped and counted
+    "overflow_bf16": W.WORKLOADS["v2lite"].with_(C=3),
+    "overflow_fp8": W.WORKLOADS["dsv3_fp8"].with_(T=200, C=2),
+    "overflow_skew": W.WORKLOADS["mixtral_skew"].with_(T=512, C=100),
+    # k extremes
+    "k1": W.WORKLOADS["v2lite"].with_(k=1),
+    "k_eq_E": W.WORKLOADS["tiny"].with_(k=8),
+    # expert counts not a multiple of 32 / of 4, smallest and largest
+    "E100": W.Workload("E100", T=130, H=64, E=100, k=5, R=4, C=40, seed=7),
+    "E1": W.Workload("E1", T=40, H=16, E=1, k=1, R=1, C=64, seed=8),
+    "E6": W.Workload("E6", T=50, H=8, E=6, k=3, R=3, C=50, seed=9),
+    "E1024_k16_fp8": W.Workload("E1024", T=100, H=128, E=1024, k=16, R=8, C=16, dtype=1, seed=10),
+    # hidden extremes
+    "H8": W.Workload("H8", T=64, H=8, E=8, k=2, R=2, C=64, seed=11),
+    "H65536": W.Workload("H65536", T=3, H=65536, E=4, k=2, R=2, C=4, seed=12),
+    "H128_fp8": W.Workload("H128", T=64, H=128, E=16, k=4, R=4, C=64, dtype=1, seed=13),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EDGE))
+def test_edge_case_parity(case):
+    from gpu_path import compare
+    w = EDGE[case]
+    g, o = run_both(w)
+    compare(g, o, w.C, w.dtype == W.DTYPE_FP8_E4M3_B128)
+    if case.startswith("overflow"):
+        assert o["dropped"] > 0
+
+
+def test_ties_and_signed_zeros():
+    from gpu_path import compare
+    w = W.Workload("ties", T=256, H=256, E=64, k=6, R=4, C=256, seed=21)
+    rng = np.random.default_rng(21)
+    vals = np.array([-1.0, -0.0, 0.0, 0.5, 2.0], dtype=np.float32)
+    lg = vals[rng.integers(0, len(vals), size=(w.T, w.E))]
+    g, o = run_both(w, logits=lg)
+    compare(g, o, w.C, False)
+
+
+def test_all_equal_logits_and_k_eq_E_fp8():
+    from gpu_path import compare
+    w = W.Workload("flat", T=40, H=256, E=16, k=16, R=2, C=40, dtype=1, seed=22)
+    lg = np.zeros((w.T, w.E), dtype=np.float32)
+    g, o = run_both(w, logits=lg)
+    compare(g, o, w.C, True)
+    assert np.array_equal(g["topk_idx"], np.tile(np.arange(16, dtype=np.int32), (w.T, 1)))
+
+
+def test_fp8_zero_and_tiny_blocks():
+    """All-zero blocks (scale 1, codes 0), blocks of subnormal-range values
+    and negative zeros."""
+    from gpu_path import compare
+    import torch
+    w = W.Workload("zeros", T=64, H=512, E=8, k=2, R=2, C=64, dtype=1, seed=23)
+    x = W.make_x(w)
+    x[:, :128] = 0
+    x[1::2, 128:256] = 0x8000                                   # -0.0
+    tiny = torch.tensor(np.random.default_rng(3).standard_normal((w.T, 128)) * 1e-30, dtype=torch.float32)
+    x[:, 256:384] = tiny.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    x[:, 384] = 0x3F80                                           # 1.0 next to tiny values
+    g, o = run_both(w, x=x)
+    compare(g, o, w.C, True)
+
+
+def test_nan_logits_give_in_range_distinct_indices():
+    """NaN logits: the order is unspecified, but the indices stay valid."""
+    from gpu_path import run_stages
+    w = W.Workload("nan", T=64, H=64, E=32, k=4, R=2, C=64, seed=24)
+    lg = W.make_logits(w)
+    lg[::3, ::5] = np.nan
+    g = run_stages(W.make_x(w), lg, W.expert_scale(w), w.k, w.R, w.C, False)
+    assert np.all((g["topk_idx"] >= 0) & (g["topk_idx"] < w.E))
+    assert all(len(set(r)) == w.k for r in g["topk_idx"].tolist())
+    assert int(g["counts"].sum()) == w.T * w.k
+
+
+def test_empty_batch_writes_zero_counts():
+    import torch
+    import combine_router_top_gb300 as M
+    p = M.problem(0, 256, 8, 2, 2, 16)
+    b = M.alloc_buffers(p, "cuda:0")
+    for key in ["counts", "offsets", "rank_counts", "dropped"]:
+        b[key].fill_(-7)
+    empty = torch.empty(0, device="cuda:0")
+    M.moe_route(p, empty, empty, empty, b["counts"], b["offsets"], empty, b["rank_counts"], b["dropped"], b["workspace"])
+    torch.cuda.synchronize()
+    for key in ["counts", "offsets", "rank_counts", "dropped"]:
+        assert int(b[key].abs().sum()) == 0, key
+
+
+def test_dbo_step_equals_two_single_shot_runs_and_the_oracle():
+    """[DBO §UBatchRunner] midpoint split; each micro-batch runs the whole path
+    on its own buffers, dispatch(1) on the comm stream overlapping combine(0)
+    on the compute stream. The step's output is bit-identical to two single-
+    stream runs of the halves and within 1 ulp of the oracle."""
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev, to_host, ulp_distance
+    w = W.WORKLOADS["dbo"]
+    x, lg, s = W.make_x(w), W.make_logits(w), W.expert_scale(w)
+    T0, T1 = w.T // 2, w.T - w.T // 2
+    pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C)
+    bufs = [M.alloc_buffers(M.problem(T1, w.H, w.E, w.k, w.R, w.C), "cuda:0") for _ in range(2)]
+    xd, ld, sd = to_dev(x), to_dev(lg), to_dev(s)
+    out = torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0")
+    comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    ctx = M.dbo_create()
+    comp.wait_stream(torch.cuda.current_stream())
+    M.dbo_step(ctx, pf, xd, ld, sd, bufs, out, comp, comm, record_timing=True)
+    t = M.dbo_read_timing(ctx)
+    torch.cuda.synchronize()
+    got = to_host(out, np.uint16)
+    assert 0.0 <= t["overlap_fraction"] <= 1.0 and t["step_ms"] > 0
+    # two single-shot runs of the halves on one stream
+    ref = torch.empty_like(out)
+    for (a, b) in [(0, T0), (T0, w.T)]:
+        p = M.problem(b - a, w.H, w.E, w.k, w.R, w.C)
+        bb = M.alloc_buffers(p, "cuda:0")
+        M.run_path(p, xd[a:b], ld[a:b], sd, bb, ref[a:b])
+    torch.cuda.synchronize()
+    assert np.array_equal(got, to_host(ref, np.uint16))
+    # the oracle, micro-batch by micro-batch
+    o = O.run_dbo(x, lg, s, w.k, w.R, w.C, False)
+    assert ulp_distance(got, o["out"]).max() <= 1
+    for u in range(2):
+        assert np.array_equal(to_host(bufs[u]["topk_idx"])[: o["parts"][u]["topk_idx"].shape[0]], o["parts"][u]["topk_idx"])
+        assert np.array_equal(to_host(bufs[u]["counts"]), o["parts"][u]["counts"])
+        assert np.array_equal(to_host(bufs[u]["slot"])[: o["parts"][u]["slot"].shape[0]], o["parts"][u]["slot"])
+    ctx.close()
+
+
+@pytest.mark.parametrize("T", [1, 7, 64])
+def test_dbo_small_and_odd_batches(T):
+    """Odd T puts the extra token in micro-batch 1; T = 1 leaves micro-batch 0
+    empty, which runs as an empty batch."""
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev, to_host, ulp_distance
+    w = W.WORKLOADS["tiny"].with_(T=T)
+    x, lg, s = W.make_x(w), W.make_logits(w), W.expert_scale(w)
+    pf = M.problem(T, w.H, w.E, w.k, w.R, w.C)
+    T1 = T - T // 2
+    bufs = [M.alloc_buffers(M.problem(T1, w.H, w.E, w.k, w.R, w.C), "cuda:0") for _ in range(2)]
+    out = torch.empty((T, w.H), dtype=torch.int16, device="cuda:0")
+    comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    ctx = M.dbo_create()
+    comp.wait_stream(torch.cuda.current_stream())
+    M.dbo_step(ctx, pf, to_dev(x), to_dev(lg), to_dev(s), bufs, out, comp, comm)
+    torch.cuda.synchronize()
+    o = O.run_dbo(x, lg, s, w.k, w.R, w.C, False)
+    assert ulp_distance(to_host(out, np.uint16), o["out"]).max() <= 1
+    if T == 1:
+        assert int(to_host(bufs[0]["counts"]).sum()) == 0
+    ctx.close()
