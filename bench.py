@@ -48,7 +48,7 @@ UNIT = "tokens/s"
 WORKLOAD = "dsv3_fp8"
 DTYPE = "e4m3+bf16 (fp32 arithmetic)"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 6          # route: top-k/tile, scan, slot; dispatch; expert; combine
+KERNELS_PER_STEP = 5          # route: top-k/tile + finalize; dispatch; expert; combine
 CPU_SAMPLE_TOKENS = 256       # the oracle's bounded sample: 2 of the 8 source ranks
 
 
@@ -313,8 +313,8 @@ def run_ours(args, rank: int, world: int, local: int):
     b = M.alloc_buffers(p, dev)
     out = torch.empty((w.T, w.H), dtype=torch.int16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_w = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
-    flush_r = torch.ones_like(flush_w)
+    flush_w = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones_like(flush_w)       # float32: the sum reduces in place, no widening copy
     stream = torch.cuda.current_stream()
 
     def flush():
@@ -433,8 +433,8 @@ def run_dbo(args, dev) -> dict:
     comp, comm = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ctx = M.dbo_create()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_w = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
-    flush_r = torch.ones_like(flush_w)
+    flush_w = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones_like(flush_w)       # float32: the sum reduces in place, no widening copy
     res = {"overlap_fraction": [], "step_ms": [], "dispatch_ub1_ms": [], "combine_ub0_ms": [], "serial_ms": []}
     reps = 10
     with torch.cuda.stream(comp):

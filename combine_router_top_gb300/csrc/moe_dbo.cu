@@ -73,9 +73,9 @@ extern "C" int dbo_step(moe_dbo_ctx *ctx, const moe_problem *full, const void *x
     moe_problem p[2] = {*full, *full};
     p[0].num_tokens = T0;
     p[1].num_tokens = T1;
-    // overlapped pair: at most two thread blocks per SM each
+    // overlapped pair: at most four 128-thread blocks per SM each, so that both fit
     moe_problem p_overlap[2] = {p[0], p[1]};
-    const int cap = full->max_blocks > 0 ? full->max_blocks : 2 * sm_count();
+    const int cap = full->max_blocks > 0 ? full->max_blocks : 4 * sm_count();
     p_overlap[0].max_blocks = cap;
     p_overlap[1].max_blocks = cap;
 

@@ -38,12 +38,30 @@ inline int launch_status(void) {
 }
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Thread blocks of `kernel` that fit on the whole GPU at once (occupancy x SMs).
+template <typename Kernel>
+int resident_blocks(Kernel kernel, int block, size_t smem = 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess || n < 1) n = 1;
+    return n * sm_count();
+}
+
+// Grid of a persistent kernel over `units` work units: one wave of resident
+// blocks, or fewer when max_blocks caps it or there is less work.
+inline int persistent_grid(long long units, int resident, int max_blocks) {
+    long long g = resident;
+    if (max_blocks > 0 && max_blocks < g) g = max_blocks;
+    if (units < g) g = units;
+    return g < 1 ? 1 : (int)g;
+}
+
 // ---- device helpers -------------------------------------------------------
 
-// 16-byte load through the read-only path, not kept in L1 (each row is read once).
+// 16-byte load through the read-only path, not kept in L1 (each row is read
+// once). Only for data no kernel writes while this one runs.
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
     return r;
@@ -51,8 +69,7 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
 
 __device__ __forceinline__ void st_v4(void *p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
+                 "r"(v.w));
 }
 
 // bf16 pair in a 32-bit word -> two floats (exact: bf16 is the upper half of a binary32).

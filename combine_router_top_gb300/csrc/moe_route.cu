@@ -7,16 +7,17 @@
 // tokens per destination expert. [PMC §Portable kernels]: a fixed per-expert
 // bound lets every sender compute a unique destination address.
 //
-// Three launches, no atomics that decide an order:
+// Two launches, no atomics that decide an order:
 //   K1 route_topk_tile: one CTA per tile of 32 tokens, one warp per token.
 //      Top-k by k rounds of a warp arg-max (redux.sync max on an order-
 //      preserving 32-bit key, ballot for the lowest tied lane). Weights by
 //      expf and one IEEE division. Each chosen expert sets the token's bit in
 //      a per-expert 32-bit shared-memory mask; a pair's rank within the tile is
 //      the popcount of the lower bits, the tile's count per expert the popcount.
-//   K2 route_scan: one CTA. Exclusive scan over tiles per expert (tile bases,
-//      in place in the workspace), totals, offsets, rank counts, drops.
-//   K3 route_slot: slot = tile base + rank in tile, or -1 beyond capacity.
+//   K2 route_finalize: one CTA per tile. The tile's per-expert base is the
+//      sum of the earlier tiles' counts; slot = base + rank in tile, or -1 at
+//      or past the capacity. The last CTA also forms the totals, offsets,
+//      rank counts and drops.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -96,45 +97,54 @@ route_topk_tile_kernel(const float *__restrict__ logits, int T, int E, int k,
         tile_counts[(size_t)tile * E + e] = __popc(mask[e]);
 }
 
+// CTA b finalises tile b: its per-expert base is the sum of the counts of
+// tiles 0..b-1 (read from the workspace; 1024/E thread groups split the
+// tiles), slot = base + rank in tile (or -1 at or past C). The last CTA also
+// adds its own tile to get the totals and writes counts, offsets,
+// rank_counts and dropped.
 __global__ void __launch_bounds__(1024, 1)
-route_scan_kernel(int n_tiles, int E, int R, int C, int32_t *__restrict__ wc,
-                  int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                  int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped) {
+route_finalize_kernel(int T, int n_tiles, int E, int k, int R, int C, const int32_t *__restrict__ tile_counts,
+                      const int32_t *__restrict__ topk_idx, int32_t *__restrict__ slot,
+                      int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                      int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped) {
     __shared__ int32_t part[1024];
-    __shared__ int32_t tot[kMaxExperts];
+    __shared__ int32_t base[kMaxExperts];
     __shared__ int32_t racc[kMaxExperts];
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t dacc;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int G = (1024 / E) > 0 ? (1024 / E) : 1;   // groups of E threads split the tiles
+    const int b = blockIdx.x;
+    const bool last = b == (int)gridDim.x - 1;
+    const int G = (1024 / E) > 0 ? (1024 / E) : 1;
     const int g = tid / E, e = tid % E;
-    const bool on = g < G;
-    const int per = (n_tiles + G - 1) / G;
-    const int b0 = min(n_tiles, g * per), b1 = min(n_tiles, b0 + per);
-
-    if (on) {
+    if (g < G) {
         int s = 0;
 #pragma unroll 8
-        for (int b = b0; b < b1; ++b) s += wc[(size_t)b * E + e];
+        for (int tt = g; tt < b; tt += G) s += __ldg(tile_counts + (size_t)tt * E + e);
         part[tid] = s;
     }
-    for (int i = tid; i < E; i += blockDim.x) racc[i] = 0;
-    if (tid == 0) dacc = 0;
-    __syncthreads();
-    if (on) {
-        int run = 0;
-        for (int gg = 0; gg < g; ++gg) run += part[gg * E + e];
-        for (int b = b0; b < b1; ++b) {
-            const int c = wc[(size_t)b * E + e];
-            wc[(size_t)b * E + e] = run;
-            run += c;
-        }
-        if (g == G - 1) tot[e] = run;
+    if (last) {
+        for (int i = tid; i < E; i += blockDim.x) racc[i] = 0;
+        if (tid == 0) dacc = 0;
     }
     __syncthreads();
+    if (tid < E) {
+        int s = 0;
+        for (int gg = 0; gg < G; ++gg) s += part[gg * E + tid];
+        base[tid] = s;
+    }
+    __syncthreads();
+    const int t0 = b * kTileTokens;
+    const int n_pairs = (min(T - t0, kTileTokens) > 0 ? min(T - t0, kTileTokens) : 0) * k;
+    for (int i = tid; i < n_pairs; i += blockDim.x) {
+        const size_t gi = (size_t)t0 * k + i;
+        const int s = base[__ldg(topk_idx + gi)] + slot[gi];
+        slot[gi] = s < C ? s : -1;
+    }
+    if (!last) return;                                   // block-uniform
 
-    // offsets = exclusive scan of the totals over experts
-    const int v = tid < E ? tot[tid] : 0;
+    // totals = base of this (last) tile + its own counts
+    const int v = tid < E ? base[tid] + (b < n_tiles ? __ldg(tile_counts + (size_t)b * E + tid) : 0) : 0;
     int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -164,17 +174,6 @@ route_scan_kernel(int n_tiles, int E, int R, int C, int32_t *__restrict__ wc,
     __syncthreads();
     for (int r = tid; r < R; r += blockDim.x) rank_counts[r] = racc[r];
     if (tid == 0) *dropped = dacc;
-}
-
-__global__ void route_slot_kernel(int n_pairs, int k, int E, int C,
-                                  const int32_t *__restrict__ topk_idx,
-                                  const int32_t *__restrict__ tile_base,
-                                  int32_t *__restrict__ slot) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n_pairs) return;
-    const int tile = (i / k) / kTileTokens;
-    const int s = tile_base[(size_t)tile * E + topk_idx[i]] + slot[i];
-    slot[i] = s < C ? s : -1;
 }
 
 template <int V>
@@ -217,10 +216,8 @@ extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *top
         else if (per_lane <= 16) launch_topk<16>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
         else launch_topk<32>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
     }
-    route_scan_kernel<<<1, 1024, 0, st>>>(n_tiles, d.E, d.R, d.C, wc, counts, offsets, rank_counts, dropped);
-    if (d.T > 0) {
-        const int n_pairs = d.T * d.k;
-        route_slot_kernel<<<(n_pairs + 255) / 256, 256, 0, st>>>(n_pairs, d.k, d.E, d.C, topk_idx, wc, slot);
-    }
+    // an empty batch still runs one finalise block: it writes the zero counts
+    route_finalize_kernel<<<n_tiles > 0 ? n_tiles : 1, 1024, 0, st>>>(d.T, n_tiles, d.E, d.k, d.R, d.C, wc, topk_idx,
+                                                                     slot, counts, offsets, rank_counts, dropped);
     return launch_status();
 }
