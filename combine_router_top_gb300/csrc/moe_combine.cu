@@ -8,15 +8,13 @@
 //   out[t] = bf16( fma-accumulate_{j ascending, slot >= 0} w[t][j] * y[e_j][slot_j] )
 //
 // Both kernels are persistent: one wave of resident thread blocks walks a
-// list of small work units, so that no partial second wave idles SMs.
-//   combine: unit = (token, 128 consecutive 16-byte chunks of its row). A
-//     thread owns one chunk: it issues the k gathers, then k fp32 FMAs in
-//     ascending j, then one 16-byte bf16 store. Warp 0 loads the next unit's
-//     routing (row, weight) into the other half of a double buffer while the
-//     block works on the current one.
-//   expert: unit = (kept row, segment of the row). Kept rows are enumerated
-//     compactly through an exclusive scan of min(counts[e], C) held in
-//     shared memory, so no block walks empty capacity rows.
+// list of small work units, so that no partial second wave idles SMs, and
+// no block-wide barrier sits in the steady-state loop.
+//   combine: every warp walks its own units (token, 32 chunks of 16 bytes);
+//     the routing of a token is held by lanes j < k and broadcast by shuffle.
+//   expert: tasks (kept row, 16-byte piece) are numbered over the kept rows
+//     only, through an exclusive scan of min(counts[e], C) held in shared
+//     memory, so no thread walks empty capacity rows.
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -24,80 +22,86 @@
 namespace moe {
 namespace {
 
-constexpr int kCombineBlock = 128;
+constexpr int kBlock = 256;                  // 8 warps; every warp walks its own work units
+constexpr int kWarps = kBlock / 32;
 
-// Warp 0: compacted (row offset in 16-byte units, weight) of token t's kept
-// choices, ascending j. The three loads of a lane are independent.
-template <int KMAX>
-__device__ __forceinline__ void combine_routing(int t, int k, int C, int H8, const int32_t *__restrict__ topk_idx,
-                                                const float *__restrict__ topk_w, const int32_t *__restrict__ slot,
-                                                long long *rows, float *ws, int *n) {
-    const int lane = threadIdx.x;
-    int s = -1, e = 0;
-    float w = 0.0f;
+// Lane j < k of a warp holds choice j of token t: slot, expert, weight.
+struct Choice {
+    int s, e;
+    float w;
+};
+__device__ __forceinline__ Choice load_choice(int t, int k, const int32_t *__restrict__ topk_idx,
+                                              const float *__restrict__ topk_w, const int32_t *__restrict__ slot) {
+    Choice c{-1, 0, 0.0f};
+    const int lane = threadIdx.x & 31;
     if (lane < k) {
-        s = __ldg(slot + (size_t)t * k + lane);
-        e = __ldg(topk_idx + (size_t)t * k + lane);
-        w = __ldg(topk_w + (size_t)t * k + lane);
+        c.s = __ldg(slot + (size_t)t * k + lane);
+        c.e = __ldg(topk_idx + (size_t)t * k + lane);
+        c.w = __ldg(topk_w + (size_t)t * k + lane);
     }
-    const unsigned kept = __ballot_sync(kFull, s >= 0);
-    if (s >= 0) {
-        const int pos = __popc(kept & ((1u << lane) - 1u));
-        rows[pos] = ((long long)e * C + s) * H8;
-        ws[pos] = w;
-    }
-    if (lane == 0) *n = __popc(kept);
+    return c;
 }
 
+// Unit = (token, 32 consecutive 16-byte chunks of its row): lane l owns chunk
+// 32*seg + l. The warp broadcasts each kept choice (ascending j) by shuffle,
+// issues all gathers, then accumulates in fp32 in ascending j. The next
+// unit's routing is loaded before the current unit's gathers are issued.
 template <int KMAX>
-__global__ void __launch_bounds__(kCombineBlock)
+__global__ void __launch_bounds__(kBlock, KMAX <= 8 ? 4 : 2)
 combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ topk_idx,
                const float *__restrict__ topk_w, const int32_t *__restrict__ slot,
                uint4 *__restrict__ out, int T, int H8, int k, int C, int segs) {
-    __shared__ long long s_row[2][KMAX];
-    __shared__ float s_w[2][KMAX];
-    __shared__ int s_n[2];
+    const int lane = threadIdx.x & 31;
     const long long n_units = (long long)T * segs;
-    long long u = blockIdx.x;
-    if (u >= n_units) return;
-    if (threadIdx.x < 32)
-        combine_routing<KMAX>((int)(u / segs), k, C, H8, topk_idx, topk_w, slot, s_row[0], s_w[0], &s_n[0]);
-    __syncthreads();
-    int b = 0;
-    for (; u < n_units; u += gridDim.x) {
-        const long long un = u + gridDim.x;
-        if (un < n_units && threadIdx.x < 32)
-            combine_routing<KMAX>((int)(un / segs), k, C, H8, topk_idx, topk_w, slot, s_row[b ^ 1], s_w[b ^ 1],
-                                  &s_n[b ^ 1]);
+    const long long stride = (long long)gridDim.x * kWarps;
+    long long u = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (u >= n_units) return;                                  // warp-uniform
+    Choice cur = load_choice((int)(u / segs), k, topk_idx, topk_w, slot);
+    for (; u < n_units; u += stride) {
+        const long long un = u + stride;
+        Choice nxt{-1, 0, 0.0f};
+        if (un < n_units) nxt = load_choice((int)(un / segs), k, topk_idx, topk_w, slot);
         const int t = (int)(u / segs);
-        const int c = (int)(u % segs) * kCombineBlock + threadIdx.x;
-        const int ns = s_n[b];
-        if (c < H8) {
-            uint4 v[KMAX];
+        const int c = (int)(u % segs) * 32 + lane;
+        const bool on = c < H8;
+        const long long my_row = ((long long)cur.e * C + (cur.s >= 0 ? cur.s : 0)) * H8;
+        const unsigned kept = __ballot_sync(kFull, cur.s >= 0);
+        const int n_kept = __popc(kept);
+        uint4 v[KMAX];
+        unsigned rem = kept;
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-                if (j < ns) v[j] = ld_stream_v4(y + s_row[b][j] + c);
-            float acc[8];
+        for (int j = 0; j < KMAX; ++j) {
+            if (j < n_kept) {                                  // warp-uniform
+                const int src = __ffs(rem) - 1;
+                rem &= rem - 1;
+                const long long row = __shfl_sync(kFull, my_row, src);
+                if (on) v[j] = ld_stream_v4(y + row + c);
+            }
+        }
+        float acc[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        rem = kept;
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) {
-                if (j < ns) {
-                    const float w = s_w[b][j];
-                    const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        for (int j = 0; j < KMAX; ++j) {
+            if (j < n_kept) {                                  // warp-uniform
+                const int src = __ffs(rem) - 1;
+                rem &= rem - 1;
+                const float w = __shfl_sync(kFull, cur.w, src);
+                const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        acc[2 * i] = __fmaf_rn(w, bf16_lo(wv[i]), acc[2 * i]);
-                        acc[2 * i + 1] = __fmaf_rn(w, bf16_hi(wv[i]), acc[2 * i + 1]);
-                    }
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = __fmaf_rn(w, bf16_lo(wv[i]), acc[2 * i]);
+                    acc[2 * i + 1] = __fmaf_rn(w, bf16_hi(wv[i]), acc[2 * i + 1]);
                 }
             }
+        }
+        if (on) {
             st_v4(out + (size_t)t * H8 + c,
                   make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                              pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
         }
-        __syncthreads();   // current buffer consumed, next one filled
-        b ^= 1;
+        cur = nxt;
     }
 }
 
@@ -139,7 +143,7 @@ __device__ void kept_row_offsets(const int32_t *__restrict__ counts, int E, int 
     __syncthreads();
 }
 
-// Expert e of kept row p: the last e with off[e] <= p (off is non-decreasing).
+// Expert of kept row p: the last e with off[e] <= p (off is non-decreasing).
 __device__ __forceinline__ int expert_of_row(const int32_t *off, int E, int p) {
     int lo = 0, hi = E;        // off[lo] <= p < off[hi]
     while (hi - lo > 1) {
@@ -149,30 +153,45 @@ __device__ __forceinline__ int expert_of_row(const int32_t *off, int E, int p) {
     return lo;
 }
 
-constexpr int kExpertBf16Block = 128;   // one 16-byte chunk (8 bf16) per thread per unit
-constexpr int kExpertFp8Block = 64;     // 16 e4m3 codes per thread per unit
+constexpr int kExpertBatch = 4;   // tasks per thread whose loads are in flight together
 
-__global__ void __launch_bounds__(kExpertBf16Block)
+// Synthetic expert, bf16 rows. Tasks (kept row, 16-byte chunk) are numbered
+// row-major over the kept rows; consecutive threads take consecutive tasks
+// (coalesced), a thread issues kExpertBatch loads before its first store.
+__global__ void __launch_bounds__(kBlock)
 expert_bf16_kernel(const uint4 *__restrict__ recv, const int32_t *__restrict__ counts,
-                   const float *__restrict__ s, uint4 *__restrict__ y, int E, int C, int H8, int segs) {
+                   const float *__restrict__ s, uint4 *__restrict__ y, int E, int C, int H8) {
     __shared__ int32_t off[kMaxExperts + 1];
     __shared__ int32_t warp_tot[32];
     kept_row_offsets(counts, E, C, off, warp_tot);
-    const long long n_units = (long long)off[E] * segs;
-    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int p = (int)(u / segs);
-        const int e = expert_of_row(off, E, p);
-        const long long row = (long long)e * C + (p - off[e]);
-        const int c = (int)(u % segs) * kExpertBf16Block + threadIdx.x;
-        if (c < H8) {
-            const float se = __ldg(s + e);
-            const uint4 v = ld_stream_v4(recv + row * H8 + c);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            uint32_t ov[4];
+    const long long total = (long long)off[E] * H8;
+    const long long stride = (long long)gridDim.x * kBlock;
+    for (long long g0 = (long long)blockIdx.x * kBlock + threadIdx.x; g0 < total; g0 += stride * kExpertBatch) {
+        uint4 v[kExpertBatch];
+        long long at[kExpertBatch];
+        float se[kExpertBatch];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                ov[i] = pack_bf16x2(__fmul_rn(bf16_lo(wv[i]), se), __fmul_rn(bf16_hi(wv[i]), se));
-            st_v4(y + row * H8 + c, make_uint4(ov[0], ov[1], ov[2], ov[3]));
+        for (int i = 0; i < kExpertBatch; ++i) {
+            const long long g = g0 + i * stride;
+            at[i] = -1;
+            if (g < total) {
+                const int p = (int)(g / H8);
+                const int e = expert_of_row(off, E, p);
+                at[i] = ((long long)e * C + (p - off[e])) * H8 + (g % H8);
+                se[i] = __ldg(s + e);
+                v[i] = ld_stream_v4(recv + at[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kExpertBatch; ++i) {
+            if (at[i] >= 0) {
+                const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                uint32_t ov[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    ov[h] = pack_bf16x2(__fmul_rn(bf16_lo(wv[h]), se[i]), __fmul_rn(bf16_hi(wv[h]), se[i]));
+                st_v4(y + at[i], make_uint4(ov[0], ov[1], ov[2], ov[3]));
+            }
         }
     }
 }
@@ -183,39 +202,55 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
     return __half2float(*reinterpret_cast<const __half *>(&h));
 }
 
-__global__ void __launch_bounds__(kExpertFp8Block)
+// Synthetic expert, fp8 rows: a task is 16 codes (16 bytes in, 32 bytes of bf16 out).
+__global__ void __launch_bounds__(kBlock)
 expert_fp8_kernel(const uint4 *__restrict__ recv_q, const float *__restrict__ recv_scale,
                   const int32_t *__restrict__ counts, const float *__restrict__ s,
-                  uint4 *__restrict__ y, int E, int C, int H, int segs) {
+                  uint4 *__restrict__ y, int E, int C, int H) {
     __shared__ int32_t off[kMaxExperts + 1];
     __shared__ int32_t warp_tot[32];
     kept_row_offsets(counts, E, C, off, warp_tot);
     const int n_tasks = H / 16, nb = H / 128;
-    const long long n_units = (long long)off[E] * segs;
-    for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int p = (int)(u / segs);
-        const int e = expert_of_row(off, E, p);
-        const long long row = (long long)e * C + (p - off[e]);
-        const int task = (int)(u % segs) * kExpertFp8Block + threadIdx.x;
-        if (task < n_tasks) {
-            const float se = __ldg(s + e);
-            const uint4 q = ld_stream_v4(recv_q + row * n_tasks + task);
-            const float sc = __ldg(recv_scale + row * nb + (task >> 3));
-            const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-            uint32_t ov[8];
+    const long long total = (long long)off[E] * n_tasks;
+    const long long stride = (long long)gridDim.x * kBlock;
+    for (long long g0 = (long long)blockIdx.x * kBlock + threadIdx.x; g0 < total; g0 += stride * kExpertBatch) {
+        uint4 q[kExpertBatch];
+        float sc[kExpertBatch], se[kExpertBatch];
+        long long row[kExpertBatch];
+        int task[kExpertBatch];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t two = qw[i] >> (16 * h);
-                    const float a = __fmul_rn(__fmul_rn(e4m3_to_float(two & 0xFFu), sc), se);
-                    const float b = __fmul_rn(__fmul_rn(e4m3_to_float((two >> 8) & 0xFFu), sc), se);
-                    ov[2 * i + h] = pack_bf16x2(a, b);
-                }
+        for (int i = 0; i < kExpertBatch; ++i) {
+            const long long g = g0 + i * stride;
+            row[i] = -1;
+            if (g < total) {
+                const int p = (int)(g / n_tasks);
+                task[i] = (int)(g % n_tasks);
+                const int e = expert_of_row(off, E, p);
+                row[i] = (long long)e * C + (p - off[e]);
+                se[i] = __ldg(s + e);
+                q[i] = ld_stream_v4(recv_q + row[i] * n_tasks + task[i]);
+                sc[i] = __ldg(recv_scale + row[i] * nb + (task[i] >> 3));
             }
-            uint4 *o = y + row * (H / 8) + 2 * task;
-            st_v4(o, make_uint4(ov[0], ov[1], ov[2], ov[3]));
-            st_v4(o + 1, make_uint4(ov[4], ov[5], ov[6], ov[7]));
+        }
+#pragma unroll
+        for (int i = 0; i < kExpertBatch; ++i) {
+            if (row[i] >= 0) {
+                const uint32_t qw[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+                uint32_t ov[8];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t two = qw[w] >> (16 * h);
+                        const float a = __fmul_rn(__fmul_rn(e4m3_to_float(two & 0xFFu), sc[i]), se[i]);
+                        const float b = __fmul_rn(__fmul_rn(e4m3_to_float((two >> 8) & 0xFFu), sc[i]), se[i]);
+                        ov[2 * w + h] = pack_bf16x2(a, b);
+                    }
+                }
+                uint4 *o = y + row[i] * (H / 8) + 2 * task[i];
+                st_v4(o, make_uint4(ov[0], ov[1], ov[2], ov[3]));
+                st_v4(o + 1, make_uint4(ov[4], ov[5], ov[6], ov[7]));
+            }
         }
     }
 }
@@ -240,17 +275,19 @@ extern "C" int moe_expert_synthetic(const moe_problem *p, const void *recv, cons
     const long long max_rows = std::min<long long>((long long)d.T * d.k, (long long)d.E * d.C);
     cudaStream_t st = as_stream(stream);
     if (fp8) {
-        static int resident = resident_blocks(expert_fp8_kernel, kExpertFp8Block);
-        const int segs = (d.H / 16 + kExpertFp8Block - 1) / kExpertFp8Block;
-        const int grid = persistent_grid(max_rows * segs, resident, d.max_blocks);
-        expert_fp8_kernel<<<grid, kExpertFp8Block, 0, st>>>(static_cast<const uint4 *>(recv), recv_scale, counts, s,
-                                                            static_cast<uint4 *>(y), d.E, d.C, d.H, segs);
+        static int resident = resident_blocks(expert_fp8_kernel, kBlock);
+        const long long tasks = max_rows * (d.H / 16);
+        const int grid = persistent_grid((tasks + (long long)kBlock * kExpertBatch - 1) / ((long long)kBlock * kExpertBatch),
+                                         resident, d.max_blocks);
+        expert_fp8_kernel<<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(recv), recv_scale, counts, s,
+                                                   static_cast<uint4 *>(y), d.E, d.C, d.H);
     } else {
-        static int resident = resident_blocks(expert_bf16_kernel, kExpertBf16Block);
-        const int segs = (d.H / 8 + kExpertBf16Block - 1) / kExpertBf16Block;
-        const int grid = persistent_grid(max_rows * segs, resident, d.max_blocks);
-        expert_bf16_kernel<<<grid, kExpertBf16Block, 0, st>>>(static_cast<const uint4 *>(recv), counts, s,
-                                                              static_cast<uint4 *>(y), d.E, d.C, d.H / 8, segs);
+        static int resident = resident_blocks(expert_bf16_kernel, kBlock);
+        const long long tasks = max_rows * (d.H / 8);
+        const int grid = persistent_grid((tasks + (long long)kBlock * kExpertBatch - 1) / ((long long)kBlock * kExpertBatch),
+                                         resident, d.max_blocks);
+        expert_bf16_kernel<<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(recv), counts, s,
+                                                    static_cast<uint4 *>(y), d.E, d.C, d.H / 8);
     }
     return launch_status();
 }
@@ -260,11 +297,12 @@ template <int KMAX>
 int launch_combine(const moe::Dims &d, cudaStream_t st, const uint4 *y, const int32_t *idx, const float *w,
                    const int32_t *slot, uint4 *out) {
     using namespace moe;
-    static int resident = resident_blocks(combine_kernel<KMAX>, kCombineBlock);
+    static int resident = resident_blocks(combine_kernel<KMAX>, kBlock);
     const int H8 = d.H / 8;
-    const int segs = (H8 + kCombineBlock - 1) / kCombineBlock;
-    const int grid = persistent_grid((long long)d.T * segs, resident, d.max_blocks);
-    combine_kernel<KMAX><<<grid, kCombineBlock, 0, st>>>(y, idx, w, slot, out, d.T, H8, d.k, d.C, segs);
+    const int segs = (H8 + 31) / 32;
+    const long long units = (long long)d.T * segs;
+    const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
+    combine_kernel<KMAX><<<grid, kBlock, 0, st>>>(y, idx, w, slot, out, d.T, H8, d.k, d.C, segs);
     return launch_status();
 }
 }  // namespace

@@ -10,104 +10,121 @@
 // the expert's rows of this HBM, at the address the slot fixes; no counts have
 // to be awaited because moe_route already produced them.
 //
-// Persistent kernels: one wave of resident thread blocks walks the work units
-// (token, 1024-element segment of its row), so no partial second wave idles
-// SMs. Warp 0 gathers the kept destination rows (ascending j) of the next
-// unit into the other half of a shared-memory double buffer while the block
-// copies the current one, and writes recv_src on a token's first segment.
-// A thread reads its part of the row once and stores it to every
-// destination. fp8: a thread quantises 16 elements; the 8 threads of one
-// 128-element block agree on amax with 3 shuffles.
+// Persistent kernels: one wave of resident thread blocks; every warp walks
+// its own work units (token, segment of its row) with no block-wide barrier.
+// Lanes j < k hold the token's destination rows and broadcast them by
+// shuffle (ascending j). The next unit's routing and row data are loaded
+// before the current unit is stored, so that two units' loads are in flight.
+// recv_src is written on a token's first segment.
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-// Warp 0: compacted destination rows (ascending j) of token t; on the token's
-// first segment also records the origin of each row.
-__device__ __forceinline__ void dispatch_routing(int t, bool first_seg, int k, int C,
-                                                 const int32_t *__restrict__ topk_idx,
-                                                 const int32_t *__restrict__ slot, long long *rows, int *n,
-                                                 int32_t *__restrict__ recv_src) {
-    const int lane = threadIdx.x;
-    int s = -1, e = 0;
+constexpr int kBlock = 256;             // 8 warps; every warp walks its own work units
+constexpr int kWarps = kBlock / 32;
+
+// Lane j < k holds choice j of token t (slot, expert).
+struct Dest {
+    int s, e;
+};
+__device__ __forceinline__ Dest load_dest(int t, int k, const int32_t *__restrict__ topk_idx,
+                                          const int32_t *__restrict__ slot) {
+    Dest d{-1, 0};
+    const int lane = threadIdx.x & 31;
     if (lane < k) {
-        s = __ldg(slot + (size_t)t * k + lane);
-        e = __ldg(topk_idx + (size_t)t * k + lane);
+        d.s = __ldg(slot + (size_t)t * k + lane);
+        d.e = __ldg(topk_idx + (size_t)t * k + lane);
     }
-    const unsigned kept = __ballot_sync(kFull, s >= 0);
-    if (s >= 0) {
-        const long long row = (long long)e * C + s;
-        rows[__popc(kept & ((1u << lane) - 1u))] = row;
-        if (first_seg) recv_src[row] = t;
-    }
-    if (lane == 0) *n = __popc(kept);
+    return d;
 }
 
-constexpr int kDispatchBf16Block = 128;   // 16-byte chunk (8 elements) per thread per unit
-constexpr int kDispatchFp8Block = 64;     // 16 elements per thread per unit
-
-__global__ void __launch_bounds__(kDispatchBf16Block)
+// bf16: unit = (token, 64 consecutive 16-byte chunks); lane l owns chunks
+// 64*seg + l and 64*seg + 32 + l.
+__global__ void __launch_bounds__(kBlock)
 dispatch_bf16_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
                      const int32_t *__restrict__ slot, uint4 *__restrict__ recv,
                      int32_t *__restrict__ recv_src, int T, int H8, int k, int C, int segs) {
-    __shared__ long long s_row[2][kMaxTopK];
-    __shared__ int s_n[2];
+    const int lane = threadIdx.x & 31;
     const long long n_units = (long long)T * segs;
-    long long u = blockIdx.x;
-    if (u >= n_units) return;
-    if (threadIdx.x < 32)
-        dispatch_routing((int)(u / segs), u % segs == 0, k, C, topk_idx, slot, s_row[0], &s_n[0], recv_src);
-    __syncthreads();
-    int b = 0;
-    for (; u < n_units; u += gridDim.x) {
-        const long long un = u + gridDim.x;
-        if (un < n_units && threadIdx.x < 32)
-            dispatch_routing((int)(un / segs), un % segs == 0, k, C, topk_idx, slot, s_row[b ^ 1], &s_n[b ^ 1],
-                             recv_src);
-        const int t = (int)(u / segs);
-        const int c = (int)(u % segs) * kDispatchBf16Block + threadIdx.x;
-        if (c < H8) {
-            const uint4 v = ld_stream_v4(x + (size_t)t * H8 + c);
-            const int nd = s_n[b];
-            for (int j = 0; j < nd; ++j) st_v4(recv + s_row[b][j] * H8 + c, v);
+    const long long stride = (long long)gridDim.x * kWarps;
+    long long u = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (u >= n_units) return;                                      // warp-uniform
+    auto load_row = [&](long long unit, uint4 &a, uint4 &b) {
+        const int t = (int)(unit / segs), c = (int)(unit % segs) * 64 + lane;
+        const uint4 *src = x + (size_t)t * H8;
+        if (c < H8) a = ld_stream_v4(src + c);
+        if (c + 32 < H8) b = ld_stream_v4(src + c + 32);
+    };
+    Dest cur = load_dest((int)(u / segs), k, topk_idx, slot);
+    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
+    load_row(u, a0, a1);
+    for (; u < n_units; u += stride) {
+        const long long un = u + stride;
+        Dest nxt{-1, 0};
+        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0;
+        if (un < n_units) {
+            nxt = load_dest((int)(un / segs), k, topk_idx, slot);
+            load_row(un, b0, b1);
         }
-        __syncthreads();
-        b ^= 1;
+        const int t = (int)(u / segs);
+        const int sg = (int)(u % segs);
+        const int c = sg * 64 + lane;
+        const long long my_row = (long long)cur.e * C + (cur.s >= 0 ? cur.s : 0);
+        if (sg == 0 && cur.s >= 0) recv_src[my_row] = t;
+        unsigned rem = __ballot_sync(kFull, cur.s >= 0);
+        while (rem) {                                              // warp-uniform
+            const int src = __ffs(rem) - 1;
+            rem &= rem - 1;
+            uint4 *dst = recv + __shfl_sync(kFull, my_row, src) * H8;
+            if (c < H8) st_v4(dst + c, a0);
+            if (c + 32 < H8) st_v4(dst + c + 32, a1);
+        }
+        cur = nxt;
+        a0 = b0;
+        a1 = b1;
     }
 }
 
-// A task is 16 consecutive elements of a row: 32 bytes of bf16 in, 16 bytes of e4m3 out.
-__global__ void __launch_bounds__(kDispatchFp8Block)
+// fp8: unit = (token, 32 tasks of 16 elements = 512 elements); lane l owns
+// task 32*seg + l. The 8 lanes of one 128-element block agree on its amax
+// with 3 shuffles; scale = amax/448 (1 for an all-zero block); codes are
+// e4m3(x / scale), round to nearest even, saturating.
+__global__ void __launch_bounds__(kBlock)
 dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
                     const int32_t *__restrict__ slot, uint4 *__restrict__ recv_q,
                     float *__restrict__ recv_scale, int32_t *__restrict__ recv_src, int T, int H,
                     int k, int C, int segs) {
-    __shared__ long long s_row[2][kMaxTopK];
-    __shared__ int s_n[2];
+    const int lane = threadIdx.x & 31;
     const int n_tasks = H / 16, nb = H / 128;
     const long long n_units = (long long)T * segs;
-    long long u = blockIdx.x;
-    if (u >= n_units) return;
-    if (threadIdx.x < 32)
-        dispatch_routing((int)(u / segs), u % segs == 0, k, C, topk_idx, slot, s_row[0], &s_n[0], recv_src);
-    __syncthreads();
-    int b = 0;
-    for (; u < n_units; u += gridDim.x) {
-        const long long un = u + gridDim.x;
-        if (un < n_units && threadIdx.x < 32)
-            dispatch_routing((int)(un / segs), un % segs == 0, k, C, topk_idx, slot, s_row[b ^ 1], &s_n[b ^ 1],
-                             recv_src);
-        const int t = (int)(u / segs);
-        const int task = (int)(u % segs) * kDispatchFp8Block + threadIdx.x;
-        const bool on = task < n_tasks;            // uniform over each 8-thread block group
-        uint4 a = make_uint4(0, 0, 0, 0), c = a;
-        if (on) {
+    const long long stride = (long long)gridDim.x * kWarps;
+    long long u = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (u >= n_units) return;                                      // warp-uniform
+    auto load_task = [&](long long unit, uint4 &a, uint4 &b) {
+        const int t = (int)(unit / segs), task = (int)(unit % segs) * 32 + lane;
+        if (task < n_tasks) {
             const uint4 *src = x + (size_t)t * (H / 8) + 2 * task;
             a = ld_stream_v4(src);
-            c = ld_stream_v4(src + 1);
+            b = ld_stream_v4(src + 1);
         }
-        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    };
+    Dest cur = load_dest((int)(u / segs), k, topk_idx, slot);
+    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
+    load_task(u, a0, a1);
+    for (; u < n_units; u += stride) {
+        const long long un = u + stride;
+        Dest nxt{-1, 0};
+        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0;
+        if (un < n_units) {
+            nxt = load_dest((int)(un / segs), k, topk_idx, slot);
+            load_task(un, b0, b1);
+        }
+        const int t = (int)(u / segs);
+        const int sg = (int)(u % segs);
+        const int task = sg * 32 + lane;
+        const bool on = task < n_tasks;                            // uniform per 8-lane block
+        const uint32_t wv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         float f[16];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -117,7 +134,6 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ top
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-        // the 8 threads of one 128-element block (lanes 8g .. 8g+7)
         amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
         amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
@@ -129,17 +145,22 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ top
             const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * i + 2], scale), __fdiv_rn(f[4 * i + 3], scale));
             q[i] = lo | (hi << 16);
         }
-        if (on) {
-            const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
-            const int nd = s_n[b];
-            for (int j = 0; j < nd; ++j) {
-                const long long row = s_row[b][j];
+        const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+        const long long my_row = (long long)cur.e * C + (cur.s >= 0 ? cur.s : 0);
+        if (sg == 0 && cur.s >= 0) recv_src[my_row] = t;
+        unsigned rem = __ballot_sync(kFull, cur.s >= 0);
+        while (rem) {                                              // warp-uniform
+            const int src = __ffs(rem) - 1;
+            rem &= rem - 1;
+            const long long row = __shfl_sync(kFull, my_row, src);
+            if (on) {
                 st_v4(recv_q + row * n_tasks + task, qv);
-                if ((threadIdx.x & 7) == 0) recv_scale[row * nb + (task >> 3)] = scale;
+                if ((lane & 7) == 0) recv_scale[row * nb + (task >> 3)] = scale;
             }
         }
-        __syncthreads();
-        b ^= 1;
+        cur = nxt;
+        a0 = b0;
+        a1 = b1;
     }
 }
 
@@ -163,20 +184,22 @@ extern "C" int moe_dispatch(const moe_problem *p, const void *x, const int32_t *
 
     cudaStream_t st = as_stream(stream);
     if (fp8) {
-        static int resident = resident_blocks(dispatch_fp8_kernel, kDispatchFp8Block);
-        const int segs = (d.H / 16 + kDispatchFp8Block - 1) / kDispatchFp8Block;
-        const int grid = persistent_grid((long long)d.T * segs, resident, d.max_blocks);
-        dispatch_fp8_kernel<<<grid, kDispatchFp8Block, 0, st>>>(static_cast<const uint4 *>(x), topk_idx, slot,
-                                                                static_cast<uint4 *>(recv), recv_scale, recv_src,
-                                                                d.T, d.H, d.k, d.C, segs);
+        static int resident = resident_blocks(dispatch_fp8_kernel, kBlock);
+        const int segs = (d.H / 16 + 31) / 32;
+        const long long units = (long long)d.T * segs;
+        const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
+        dispatch_fp8_kernel<<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(x), topk_idx, slot,
+                                                     static_cast<uint4 *>(recv), recv_scale, recv_src, d.T, d.H,
+                                                     d.k, d.C, segs);
     } else {
-        static int resident = resident_blocks(dispatch_bf16_kernel, kDispatchBf16Block);
+        static int resident = resident_blocks(dispatch_bf16_kernel, kBlock);
         const int H8 = d.H / 8;
-        const int segs = (H8 + kDispatchBf16Block - 1) / kDispatchBf16Block;
-        const int grid = persistent_grid((long long)d.T * segs, resident, d.max_blocks);
-        dispatch_bf16_kernel<<<grid, kDispatchBf16Block, 0, st>>>(static_cast<const uint4 *>(x), topk_idx, slot,
-                                                                  static_cast<uint4 *>(recv), recv_src, d.T, H8,
-                                                                  d.k, d.C, segs);
+        const int segs = (H8 + 63) / 64;
+        const long long units = (long long)d.T * segs;
+        const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
+        dispatch_bf16_kernel<<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(x), topk_idx, slot,
+                                                      static_cast<uint4 *>(recv), recv_src, d.T, H8, d.k, d.C,
+                                                      segs);
     }
     return launch_status();
 }
