@@ -25,21 +25,18 @@ namespace {
 constexpr int kBlock = 256;                  // 8 warps; every warp walks its own work units
 constexpr int kWarps = kBlock / 32;
 
-// Lane j < k of a warp holds choice j of token t: slot, expert, weight.
-struct Choice {
-    int s, e;
-    float w;
-};
-__device__ __forceinline__ Choice load_choice(int t, int k, const int32_t *__restrict__ topk_idx,
-                                              const float *__restrict__ topk_w, const int32_t *__restrict__ slot) {
-    Choice c{-1, 0, 0.0f};
+// Lane j < k holds choice j of token t: its source row e*C + slot (< 2^31)
+// or -1 when the pair was dropped, and its weight.
+__device__ __forceinline__ int load_choice(unsigned t, int k, int C, const int32_t *__restrict__ topk_idx,
+                                           const float *__restrict__ topk_w, const int32_t *__restrict__ slot,
+                                           float &w) {
     const int lane = threadIdx.x & 31;
-    if (lane < k) {
-        c.s = __ldg(slot + (size_t)t * k + lane);
-        c.e = __ldg(topk_idx + (size_t)t * k + lane);
-        c.w = __ldg(topk_w + (size_t)t * k + lane);
-    }
-    return c;
+    w = 0.0f;
+    if (lane >= k) return -1;
+    const int s = __ldg(slot + (size_t)t * k + lane);
+    const int e = __ldg(topk_idx + (size_t)t * k + lane);
+    w = __ldg(topk_w + (size_t)t * k + lane);
+    return s >= 0 ? e * C + s : -1;
 }
 
 // Unit = (token, 32 consecutive 16-byte chunks of its row): lane l owns chunk
@@ -52,20 +49,20 @@ combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ topk_idx
                const float *__restrict__ topk_w, const int32_t *__restrict__ slot,
                uint4 *__restrict__ out, int T, int H8, int k, int C, int segs) {
     const int lane = threadIdx.x & 31;
-    const long long n_units = (long long)T * segs;
-    const long long stride = (long long)gridDim.x * kWarps;
-    long long u = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (u >= n_units) return;                                  // warp-uniform
-    Choice cur = load_choice((int)(u / segs), k, topk_idx, topk_w, slot);
-    for (; u < n_units; u += stride) {
-        const long long un = u + stride;
-        Choice nxt{-1, 0, 0.0f};
-        if (un < n_units) nxt = load_choice((int)(un / segs), k, topk_idx, topk_w, slot);
-        const int t = (int)(u / segs);
-        const int c = (int)(u % segs) * 32 + lane;
-        const bool on = c < H8;
-        const long long my_row = ((long long)cur.e * C + (cur.s >= 0 ? cur.s : 0)) * H8;
-        const unsigned kept = __ballot_sync(kFull, cur.s >= 0);
+    UnitWalk wk(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs);
+    if (wk.row >= (unsigned)T) return;                         // warp-uniform
+    float w;
+    int src_row = load_choice(wk.row, k, C, topk_idx, topk_w, slot, w);
+    for (;;) {
+        UnitWalk nw = wk;
+        nw.next();
+        const bool more = nw.row < (unsigned)T;
+        float nwt = 0.0f;
+        int nrow = -1;
+        if (more) nrow = load_choice(nw.row, k, C, topk_idx, topk_w, slot, nwt);
+        const unsigned c = wk.seg * 32 + lane;
+        const bool on = c < (unsigned)H8;
+        const unsigned kept = __ballot_sync(kFull, src_row >= 0);
         const int n_kept = __popc(kept);
         uint4 v[KMAX];
         unsigned rem = kept;
@@ -74,8 +71,8 @@ combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ topk_idx
             if (j < n_kept) {                                  // warp-uniform
                 const int src = __ffs(rem) - 1;
                 rem &= rem - 1;
-                const long long row = __shfl_sync(kFull, my_row, src);
-                if (on) v[j] = ld_stream_v4(y + row + c);
+                const size_t row = (size_t)__shfl_sync(kFull, src_row, src);
+                if (on) v[j] = ld_stream_v4(y + row * H8 + c);
             }
         }
         float acc[8];
@@ -87,21 +84,23 @@ combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ topk_idx
             if (j < n_kept) {                                  // warp-uniform
                 const int src = __ffs(rem) - 1;
                 rem &= rem - 1;
-                const float w = __shfl_sync(kFull, cur.w, src);
+                const float wj = __shfl_sync(kFull, w, src);
                 const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = __fmaf_rn(w, bf16_lo(wv[i]), acc[2 * i]);
-                    acc[2 * i + 1] = __fmaf_rn(w, bf16_hi(wv[i]), acc[2 * i + 1]);
+                    acc[2 * i] = __fmaf_rn(wj, bf16_lo(wv[i]), acc[2 * i]);
+                    acc[2 * i + 1] = __fmaf_rn(wj, bf16_hi(wv[i]), acc[2 * i + 1]);
                 }
             }
         }
-        if (on) {
-            st_v4(out + (size_t)t * H8 + c,
+        if (on)
+            st_v4(out + (size_t)wk.row * H8 + c,
                   make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                              pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
-        }
-        cur = nxt;
+        if (!more) break;
+        wk = nw;
+        src_row = nrow;
+        w = nwt;
     }
 }
 
@@ -153,106 +152,121 @@ __device__ __forceinline__ int expert_of_row(const int32_t *off, int E, int p) {
     return lo;
 }
 
-constexpr int kExpertBatch = 4;   // tasks per thread whose loads are in flight together
-
-// Synthetic expert, bf16 rows. Tasks (kept row, 16-byte chunk) are numbered
-// row-major over the kept rows; consecutive threads take consecutive tasks
-// (coalesced), a thread issues kExpertBatch loads before its first store.
+// Synthetic expert, bf16 rows. A unit is (kept row p, 32*U consecutive
+// 16-byte chunks); kept rows are numbered through the scan above, so no
+// warp walks an empty capacity row. Lane l owns chunks 32*(U*seg + i) + l.
+template <int U>
 __global__ void __launch_bounds__(kBlock)
 expert_bf16_kernel(const uint4 *__restrict__ recv, const int32_t *__restrict__ counts,
-                   const float *__restrict__ s, uint4 *__restrict__ y, int E, int C, int H8) {
+                   const float *__restrict__ s, uint4 *__restrict__ y, int E, int C, int H8, int segs) {
     __shared__ int32_t off[kMaxExperts + 1];
     __shared__ int32_t warp_tot[32];
     kept_row_offsets(counts, E, C, off, warp_tot);
-    const long long total = (long long)off[E] * H8;
-    const long long stride = (long long)gridDim.x * kBlock;
-    for (long long g0 = (long long)blockIdx.x * kBlock + threadIdx.x; g0 < total; g0 += stride * kExpertBatch) {
-        uint4 v[kExpertBatch];
-        long long at[kExpertBatch];
-        float se[kExpertBatch];
+    const int lane = threadIdx.x & 31;
+    const unsigned rows = off[E];
+    for (UnitWalk wk(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs); wk.row < rows;
+         wk.next()) {
+        const int e = expert_of_row(off, E, (int)wk.row);
+        const size_t row = (size_t)e * C + (wk.row - off[e]);
+        const float se = __ldg(s + e);
+        const unsigned c0 = wk.seg * 32 * U + lane;
+        const uint4 *in = recv + row * H8 + c0;
+        uint4 *o = y + row * H8 + c0;
+        uint4 v[U];
 #pragma unroll
-        for (int i = 0; i < kExpertBatch; ++i) {
-            const long long g = g0 + i * stride;
-            at[i] = -1;
-            if (g < total) {
-                const int p = (int)(g / H8);
-                const int e = expert_of_row(off, E, p);
-                at[i] = ((long long)e * C + (p - off[e])) * H8 + (g % H8);
-                se[i] = __ldg(s + e);
-                v[i] = ld_stream_v4(recv + at[i]);
-            }
-        }
+        for (int i = 0; i < U; ++i)
+            if (c0 + 32 * i < (unsigned)H8) v[i] = ld_stream_v4(in + 32 * i);
 #pragma unroll
-        for (int i = 0; i < kExpertBatch; ++i) {
-            if (at[i] >= 0) {
+        for (int i = 0; i < U; ++i) {
+            if (c0 + 32 * i < (unsigned)H8) {
                 const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
                 uint32_t ov[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h)
-                    ov[h] = pack_bf16x2(__fmul_rn(bf16_lo(wv[h]), se[i]), __fmul_rn(bf16_hi(wv[h]), se[i]));
-                st_v4(y + at[i], make_uint4(ov[0], ov[1], ov[2], ov[3]));
+                    ov[h] = pack_bf16x2(__fmul_rn(bf16_lo(wv[h]), se), __fmul_rn(bf16_hi(wv[h]), se));
+                st_v4(o + 32 * i, make_uint4(ov[0], ov[1], ov[2], ov[3]));
             }
         }
     }
 }
 
-// e4m3 code -> float, exact (every e4m3 value is a binary16 and a binary32 value).
-__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
-    const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3);
-    return __half2float(*reinterpret_cast<const __half *>(&h));
+// e4m3 code pair -> two floats, exact (every e4m3 value is a binary16 value).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
-// Synthetic expert, fp8 rows: a task is 16 codes (16 bytes in, 32 bytes of bf16 out).
+// Synthetic expert, fp8 rows: a task is 16 codes (16 bytes in, 32 bytes of
+// bf16 out) with its block scale; a unit is (kept row, 32*U tasks).
+template <int U>
 __global__ void __launch_bounds__(kBlock)
 expert_fp8_kernel(const uint4 *__restrict__ recv_q, const float *__restrict__ recv_scale,
                   const int32_t *__restrict__ counts, const float *__restrict__ s,
-                  uint4 *__restrict__ y, int E, int C, int H) {
+                  uint4 *__restrict__ y, int E, int C, int H, int segs) {
     __shared__ int32_t off[kMaxExperts + 1];
     __shared__ int32_t warp_tot[32];
     kept_row_offsets(counts, E, C, off, warp_tot);
-    const int n_tasks = H / 16, nb = H / 128;
-    const long long total = (long long)off[E] * n_tasks;
-    const long long stride = (long long)gridDim.x * kBlock;
-    for (long long g0 = (long long)blockIdx.x * kBlock + threadIdx.x; g0 < total; g0 += stride * kExpertBatch) {
-        uint4 q[kExpertBatch];
-        float sc[kExpertBatch], se[kExpertBatch];
-        long long row[kExpertBatch];
-        int task[kExpertBatch];
+    const int lane = threadIdx.x & 31;
+    const unsigned n_tasks = H / 16, nb = H / 128, rows = off[E];
+    for (UnitWalk wk(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs); wk.row < rows;
+         wk.next()) {
+        const int e = expert_of_row(off, E, (int)wk.row);
+        const size_t row = (size_t)e * C + (wk.row - off[e]);
+        const float se = __ldg(s + e);
+        const unsigned t0 = wk.seg * 32 * U + lane;
+        uint4 q[U];
+        float sc[U];
 #pragma unroll
-        for (int i = 0; i < kExpertBatch; ++i) {
-            const long long g = g0 + i * stride;
-            row[i] = -1;
-            if (g < total) {
-                const int p = (int)(g / n_tasks);
-                task[i] = (int)(g % n_tasks);
-                const int e = expert_of_row(off, E, p);
-                row[i] = (long long)e * C + (p - off[e]);
-                se[i] = __ldg(s + e);
-                q[i] = ld_stream_v4(recv_q + row[i] * n_tasks + task[i]);
-                sc[i] = __ldg(recv_scale + row[i] * nb + (task[i] >> 3));
+        for (int i = 0; i < U; ++i) {
+            if (t0 + 32 * i < n_tasks) {
+                q[i] = ld_stream_v4(recv_q + row * n_tasks + t0 + 32 * i);
+                sc[i] = __ldg(recv_scale + row * nb + ((t0 + 32 * i) >> 3));
             }
         }
 #pragma unroll
-        for (int i = 0; i < kExpertBatch; ++i) {
-            if (row[i] >= 0) {
+        for (int i = 0; i < U; ++i) {
+            if (t0 + 32 * i < n_tasks) {
                 const uint32_t qw[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
                 uint32_t ov[8];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t two = qw[w] >> (16 * h);
-                        const float a = __fmul_rn(__fmul_rn(e4m3_to_float(two & 0xFFu), sc[i]), se[i]);
-                        const float b = __fmul_rn(__fmul_rn(e4m3_to_float((two >> 8) & 0xFFu), sc[i]), se[i]);
-                        ov[2 * w + h] = pack_bf16x2(a, b);
-                    }
+                for (int h = 0; h < 4; ++h) {
+                    const float2 lo = e4m3x2_to_float2(qw[h]);
+                    const float2 hi = e4m3x2_to_float2(qw[h] >> 16);
+                    ov[2 * h] = pack_bf16x2(__fmul_rn(__fmul_rn(lo.x, sc[i]), se), __fmul_rn(__fmul_rn(lo.y, sc[i]), se));
+                    ov[2 * h + 1] = pack_bf16x2(__fmul_rn(__fmul_rn(hi.x, sc[i]), se), __fmul_rn(__fmul_rn(hi.y, sc[i]), se));
                 }
-                uint4 *o = y + row[i] * (H / 8) + 2 * task[i];
+                uint4 *o = y + row * (H / 8) + 2 * (t0 + 32 * i);
                 st_v4(o, make_uint4(ov[0], ov[1], ov[2], ov[3]));
                 st_v4(o + 1, make_uint4(ov[4], ov[5], ov[6], ov[7]));
             }
         }
     }
+}
+
+template <int U>
+int launch_expert_fp8(const Dims &d, long long max_rows, cudaStream_t st, const void *recv, const float *scale,
+                      const int32_t *counts, const float *s, void *y) {
+    static int resident = resident_blocks(expert_fp8_kernel<U>, kBlock);
+    const int segs = (d.H / 16 + 32 * U - 1) / (32 * U);
+    const long long units = max_rows * segs;
+    if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
+    expert_fp8_kernel<U><<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(recv), scale, counts, s,
+                                                  static_cast<uint4 *>(y), d.E, d.C, d.H, segs);
+    return launch_status();
+}
+
+template <int U>
+int launch_expert_bf16(const Dims &d, long long max_rows, cudaStream_t st, const void *recv,
+                       const int32_t *counts, const float *s, void *y) {
+    static int resident = resident_blocks(expert_bf16_kernel<U>, kBlock);
+    const int segs = (d.H / 8 + 32 * U - 1) / (32 * U);
+    const long long units = max_rows * segs;
+    if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
+    expert_bf16_kernel<U><<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(recv), counts, s,
+                                                   static_cast<uint4 *>(y), d.E, d.C, d.H / 8, segs);
+    return launch_status();
 }
 
 }  // namespace
@@ -275,21 +289,21 @@ extern "C" int moe_expert_synthetic(const moe_problem *p, const void *recv, cons
     const long long max_rows = std::min<long long>((long long)d.T * d.k, (long long)d.E * d.C);
     cudaStream_t st = as_stream(stream);
     if (fp8) {
-        static int resident = resident_blocks(expert_fp8_kernel, kBlock);
-        const long long tasks = max_rows * (d.H / 16);
-        const int grid = persistent_grid((tasks + (long long)kBlock * kExpertBatch - 1) / ((long long)kBlock * kExpertBatch),
-                                         resident, d.max_blocks);
-        expert_fp8_kernel<<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(recv), recv_scale, counts, s,
-                                                   static_cast<uint4 *>(y), d.E, d.C, d.H);
-    } else {
-        static int resident = resident_blocks(expert_bf16_kernel, kBlock);
-        const long long tasks = max_rows * (d.H / 8);
-        const int grid = persistent_grid((tasks + (long long)kBlock * kExpertBatch - 1) / ((long long)kBlock * kExpertBatch),
-                                         resident, d.max_blocks);
-        expert_bf16_kernel<<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(recv), counts, s,
-                                                    static_cast<uint4 *>(y), d.E, d.C, d.H / 8);
+        switch (lane_tasks(d.H / 16)) {
+            case 8: return launch_expert_fp8<8>(d, max_rows, st, recv, recv_scale, counts, s, y);
+            case 7: return launch_expert_fp8<7>(d, max_rows, st, recv, recv_scale, counts, s, y);
+            case 2: return launch_expert_fp8<2>(d, max_rows, st, recv, recv_scale, counts, s, y);
+            case 1: return launch_expert_fp8<1>(d, max_rows, st, recv, recv_scale, counts, s, y);
+            default: return launch_expert_fp8<4>(d, max_rows, st, recv, recv_scale, counts, s, y);
+        }
     }
-    return launch_status();
+    switch (lane_tasks(d.H / 8)) {
+        case 8: return launch_expert_bf16<8>(d, max_rows, st, recv, counts, s, y);
+        case 7: return launch_expert_bf16<7>(d, max_rows, st, recv, counts, s, y);
+        case 2: return launch_expert_bf16<2>(d, max_rows, st, recv, counts, s, y);
+        case 1: return launch_expert_bf16<1>(d, max_rows, st, recv, counts, s, y);
+        default: return launch_expert_bf16<4>(d, max_rows, st, recv, counts, s, y);
+    }
 }
 
 namespace {
@@ -301,6 +315,7 @@ int launch_combine(const moe::Dims &d, cudaStream_t st, const uint4 *y, const in
     const int H8 = d.H / 8;
     const int segs = (H8 + 31) / 32;
     const long long units = (long long)d.T * segs;
+    if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
     combine_kernel<KMAX><<<grid, kBlock, 0, st>>>(y, idx, w, slot, out, d.T, H8, d.k, d.C, segs);
     return launch_status();

@@ -24,144 +24,192 @@ namespace {
 constexpr int kBlock = 256;             // 8 warps; every warp walks its own work units
 constexpr int kWarps = kBlock / 32;
 
-// Lane j < k holds choice j of token t (slot, expert).
-struct Dest {
-    int s, e;
-};
-__device__ __forceinline__ Dest load_dest(int t, int k, const int32_t *__restrict__ topk_idx,
-                                          const int32_t *__restrict__ slot) {
-    Dest d{-1, 0};
+// Lane j < k holds choice j of the token: its destination row e*C + slot
+// (< 2^31), or -1 when the pair was dropped.
+__device__ __forceinline__ int load_dest(unsigned t, int k, int C, const int32_t *__restrict__ topk_idx,
+                                         const int32_t *__restrict__ slot) {
     const int lane = threadIdx.x & 31;
-    if (lane < k) {
-        d.s = __ldg(slot + (size_t)t * k + lane);
-        d.e = __ldg(topk_idx + (size_t)t * k + lane);
-    }
-    return d;
+    if (lane >= k) return -1;
+    const int s = __ldg(slot + (size_t)t * k + lane);
+    const int e = __ldg(topk_idx + (size_t)t * k + lane);
+    return s >= 0 ? e * C + s : -1;
 }
 
-// bf16: unit = (token, 64 consecutive 16-byte chunks); lane l owns chunks
-// 64*seg + l and 64*seg + 32 + l.
+template <int U>
+__device__ __forceinline__ void load_fp8_tasks(const uint4 *__restrict__ x, int H, unsigned n_tasks,
+                                               const UnitWalk &at, int lane, uint4 (&v)[2 * U]) {
+    const uint4 *src = x + (size_t)at.row * (H / 8) + 2 * ((size_t)at.seg * 32 * U + lane);
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+        if (at.seg * 32 * U + 32 * i + lane < n_tasks) {
+            v[2 * i] = ld_stream_v4(src + 64 * i);
+            v[2 * i + 1] = ld_stream_v4(src + 64 * i + 1);
+        } else {
+            v[2 * i] = v[2 * i + 1] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+template <int U>
+__device__ __forceinline__ void load_bf16_chunks(const uint4 *__restrict__ x, int H8, const UnitWalk &at, int lane,
+                                                 uint4 (&v)[U]) {
+    const uint4 *src = x + (size_t)at.row * H8 + (size_t)at.seg * 32 * U + lane;
+#pragma unroll
+    for (int i = 0; i < U; ++i)
+        if (at.seg * 32 * U + 32 * i + lane < (unsigned)H8) v[i] = ld_stream_v4(src + 32 * i);
+}
+
+// bf16: a unit is (token, 32*U consecutive 16-byte chunks); lane l owns
+// chunks 32*(U*seg + i) + l, i < U.
+template <int U>
 __global__ void __launch_bounds__(kBlock)
 dispatch_bf16_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
                      const int32_t *__restrict__ slot, uint4 *__restrict__ recv,
                      int32_t *__restrict__ recv_src, int T, int H8, int k, int C, int segs) {
     const int lane = threadIdx.x & 31;
-    const long long n_units = (long long)T * segs;
-    const long long stride = (long long)gridDim.x * kWarps;
-    long long u = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (u >= n_units) return;                                      // warp-uniform
-    auto load_row = [&](long long unit, uint4 &a, uint4 &b) {
-        const int t = (int)(unit / segs), c = (int)(unit % segs) * 64 + lane;
-        const uint4 *src = x + (size_t)t * H8;
-        if (c < H8) a = ld_stream_v4(src + c);
-        if (c + 32 < H8) b = ld_stream_v4(src + c + 32);
-    };
-    Dest cur = load_dest((int)(u / segs), k, topk_idx, slot);
-    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
-    load_row(u, a0, a1);
-    for (; u < n_units; u += stride) {
-        const long long un = u + stride;
-        Dest nxt{-1, 0};
-        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0;
-        if (un < n_units) {
-            nxt = load_dest((int)(un / segs), k, topk_idx, slot);
-            load_row(un, b0, b1);
+    UnitWalk w(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs);
+    if (w.row >= (unsigned)T) return;                                  // warp-uniform
+    int dest = load_dest(w.row, k, C, topk_idx, slot);
+    uint4 a[U];
+    load_bf16_chunks<U>(x, H8, w, lane, a);
+    for (;;) {
+        UnitWalk nw = w;
+        nw.next();
+        const bool more = nw.row < (unsigned)T;
+        int ndest = -1;
+        uint4 b[U];
+        if (more) {
+            ndest = load_dest(nw.row, k, C, topk_idx, slot);
+            load_bf16_chunks<U>(x, H8, nw, lane, b);
         }
-        const int t = (int)(u / segs);
-        const int sg = (int)(u % segs);
-        const int c = sg * 64 + lane;
-        const long long my_row = (long long)cur.e * C + (cur.s >= 0 ? cur.s : 0);
-        if (sg == 0 && cur.s >= 0) recv_src[my_row] = t;
-        unsigned rem = __ballot_sync(kFull, cur.s >= 0);
-        while (rem) {                                              // warp-uniform
+        if (w.seg == 0 && dest >= 0) recv_src[dest] = (int32_t)w.row;
+        const unsigned c0 = w.seg * 32 * U + lane;
+        unsigned rem = __ballot_sync(kFull, dest >= 0);
+        while (rem) {                                                  // warp-uniform
             const int src = __ffs(rem) - 1;
             rem &= rem - 1;
-            uint4 *dst = recv + __shfl_sync(kFull, my_row, src) * H8;
-            if (c < H8) st_v4(dst + c, a0);
-            if (c + 32 < H8) st_v4(dst + c + 32, a1);
+            uint4 *dst = recv + (size_t)__shfl_sync(kFull, dest, src) * H8 + c0;
+#pragma unroll
+            for (int i = 0; i < U; ++i)
+                if (c0 + 32 * i < (unsigned)H8) st_v4(dst + 32 * i, a[i]);
         }
-        cur = nxt;
-        a0 = b0;
-        a1 = b1;
+        if (!more) break;
+        w = nw;
+        dest = ndest;
+#pragma unroll
+        for (int i = 0; i < U; ++i) a[i] = b[i];
     }
 }
 
-// fp8: unit = (token, 32 tasks of 16 elements = 512 elements); lane l owns
-// task 32*seg + l. The 8 lanes of one 128-element block agree on its amax
-// with 3 shuffles; scale = amax/448 (1 for an all-zero block); codes are
-// e4m3(x / scale), round to nearest even, saturating.
+// fp8: a task is 16 consecutive elements (32 bytes of bf16 in, 16 bytes of
+// e4m3 out); a unit is (token, 32*U tasks); lane l owns tasks
+// 32*(U*seg + i) + l, i < U. The 8 lanes of one 128-element block agree on
+// its amax with 3 shuffles; scale = amax/448 (1 for an all-zero block);
+// codes are e4m3(x / scale), round to nearest even, saturating.
+template <int U>
 __global__ void __launch_bounds__(kBlock)
 dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
                     const int32_t *__restrict__ slot, uint4 *__restrict__ recv_q,
                     float *__restrict__ recv_scale, int32_t *__restrict__ recv_src, int T, int H,
                     int k, int C, int segs) {
     const int lane = threadIdx.x & 31;
-    const int n_tasks = H / 16, nb = H / 128;
-    const long long n_units = (long long)T * segs;
-    const long long stride = (long long)gridDim.x * kWarps;
-    long long u = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (u >= n_units) return;                                      // warp-uniform
-    auto load_task = [&](long long unit, uint4 &a, uint4 &b) {
-        const int t = (int)(unit / segs), task = (int)(unit % segs) * 32 + lane;
-        if (task < n_tasks) {
-            const uint4 *src = x + (size_t)t * (H / 8) + 2 * task;
-            a = ld_stream_v4(src);
-            b = ld_stream_v4(src + 1);
+    const unsigned n_tasks = H / 16, nb = H / 128;
+    UnitWalk w(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs);
+    if (w.row >= (unsigned)T) return;                                  // warp-uniform
+    int dest = load_dest(w.row, k, C, topk_idx, slot);
+    uint4 a[2 * U];
+    load_fp8_tasks<U>(x, H, n_tasks, w, lane, a);
+    for (;;) {
+        UnitWalk nw = w;
+        nw.next();
+        const bool more = nw.row < (unsigned)T;
+        int ndest = -1;
+        uint4 b[2 * U];
+        if (more) {
+            ndest = load_dest(nw.row, k, C, topk_idx, slot);
+            load_fp8_tasks<U>(x, H, n_tasks, nw, lane, b);
         }
-    };
-    Dest cur = load_dest((int)(u / segs), k, topk_idx, slot);
-    uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
-    load_task(u, a0, a1);
-    for (; u < n_units; u += stride) {
-        const long long un = u + stride;
-        Dest nxt{-1, 0};
-        uint4 b0 = make_uint4(0, 0, 0, 0), b1 = b0;
-        if (un < n_units) {
-            nxt = load_dest((int)(un / segs), k, topk_idx, slot);
-            load_task(un, b0, b1);
-        }
-        const int t = (int)(u / segs);
-        const int sg = (int)(u % segs);
-        const int task = sg * 32 + lane;
-        const bool on = task < n_tasks;                            // uniform per 8-lane block
-        const uint32_t wv[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        float f[16];
+        uint4 qv[U];
+        float scale[U];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            f[2 * i] = bf16_lo(wv[i]);
-            f[2 * i + 1] = bf16_hi(wv[i]);
-        }
-        float amax = 0.0f;
+        for (int i = 0; i < U; ++i) {
+            const uint32_t wv[8] = {a[2 * i].x, a[2 * i].y, a[2 * i].z, a[2 * i].w,
+                                    a[2 * i + 1].x, a[2 * i + 1].y, a[2 * i + 1].z, a[2 * i + 1].w};
+            float f[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
-        const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-        uint32_t q[4];
+            for (int h = 0; h < 8; ++h) {
+                f[2 * h] = bf16_lo(wv[h]);
+                f[2 * h + 1] = bf16_hi(wv[h]);
+            }
+            float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * i], scale), __fdiv_rn(f[4 * i + 1], scale));
-            const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * i + 2], scale), __fdiv_rn(f[4 * i + 3], scale));
-            q[i] = lo | (hi << 16);
+            for (int h = 0; h < 16; ++h) amax = fmaxf(amax, fabsf(f[h]));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+            const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+            uint32_t q[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * h], sc), __fdiv_rn(f[4 * h + 1], sc));
+                const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * h + 2], sc), __fdiv_rn(f[4 * h + 3], sc));
+                q[h] = lo | (hi << 16);
+            }
+            qv[i] = make_uint4(q[0], q[1], q[2], q[3]);
+            scale[i] = sc;
         }
-        const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
-        const long long my_row = (long long)cur.e * C + (cur.s >= 0 ? cur.s : 0);
-        if (sg == 0 && cur.s >= 0) recv_src[my_row] = t;
-        unsigned rem = __ballot_sync(kFull, cur.s >= 0);
-        while (rem) {                                              // warp-uniform
+        if (w.seg == 0 && dest >= 0) recv_src[dest] = (int32_t)w.row;
+        const unsigned task0 = w.seg * 32 * U + lane;
+        unsigned rem = __ballot_sync(kFull, dest >= 0);
+        while (rem) {                                                  // warp-uniform
             const int src = __ffs(rem) - 1;
             rem &= rem - 1;
-            const long long row = __shfl_sync(kFull, my_row, src);
-            if (on) {
-                st_v4(recv_q + row * n_tasks + task, qv);
-                if ((lane & 7) == 0) recv_scale[row * nb + (task >> 3)] = scale;
+            const size_t row = (size_t)__shfl_sync(kFull, dest, src);
+            uint4 *dq = recv_q + row * n_tasks + task0;
+            float *ds = recv_scale + row * nb + (task0 >> 3);
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+                if (task0 + 32 * i < n_tasks) {
+                    st_v4(dq + 32 * i, qv[i]);
+                    if ((lane & 7) == 0) ds[4 * i] = scale[i];
+                }
             }
         }
-        cur = nxt;
-        a0 = b0;
-        a1 = b1;
+        if (!more) break;
+        w = nw;
+        dest = ndest;
+#pragma unroll
+        for (int i = 0; i < 2 * U; ++i) a[i] = b[i];
     }
+}
+
+template <int U>
+int launch_fp8(const Dims &d, cudaStream_t st, const void *x, const int32_t *idx, const int32_t *slot, void *recv,
+               float *scale, int32_t *src) {
+    static int resident = resident_blocks(dispatch_fp8_kernel<U>, kBlock);
+    const int n_tasks = d.H / 16;
+    const int segs = (n_tasks + 32 * U - 1) / (32 * U);
+    const long long units = (long long)d.T * segs;
+    if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
+    dispatch_fp8_kernel<U><<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(x), idx, slot,
+                                                    static_cast<uint4 *>(recv), scale, src, d.T, d.H, d.k, d.C,
+                                                    segs);
+    return launch_status();
+}
+
+template <int U>
+int launch_bf16(const Dims &d, cudaStream_t st, const void *x, const int32_t *idx, const int32_t *slot, void *recv,
+                int32_t *src) {
+    static int resident = resident_blocks(dispatch_bf16_kernel<U>, kBlock);
+    const int H8 = d.H / 8;
+    const int segs = (H8 + 32 * U - 1) / (32 * U);
+    const long long units = (long long)d.T * segs;
+    if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
+    dispatch_bf16_kernel<U><<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(x), idx, slot,
+                                                     static_cast<uint4 *>(recv), src, d.T, H8, d.k, d.C, segs);
+    return launch_status();
 }
 
 }  // namespace
@@ -184,22 +232,16 @@ extern "C" int moe_dispatch(const moe_problem *p, const void *x, const int32_t *
 
     cudaStream_t st = as_stream(stream);
     if (fp8) {
-        static int resident = resident_blocks(dispatch_fp8_kernel, kBlock);
-        const int segs = (d.H / 16 + 31) / 32;
-        const long long units = (long long)d.T * segs;
-        const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-        dispatch_fp8_kernel<<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(x), topk_idx, slot,
-                                                     static_cast<uint4 *>(recv), recv_scale, recv_src, d.T, d.H,
-                                                     d.k, d.C, segs);
-    } else {
-        static int resident = resident_blocks(dispatch_bf16_kernel, kBlock);
-        const int H8 = d.H / 8;
-        const int segs = (H8 + 63) / 64;
-        const long long units = (long long)d.T * segs;
-        const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-        dispatch_bf16_kernel<<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(x), topk_idx, slot,
-                                                      static_cast<uint4 *>(recv), recv_src, d.T, H8, d.k, d.C,
-                                                      segs);
+        // two tasks per lane per unit: 64 tasks = 1024 elements; the next unit's rows are prefetched
+        const int n_tasks = d.H / 16;
+        if (n_tasks % 64 == 0) return launch_fp8<2>(d, st, x, topk_idx, slot, recv, recv_scale, recv_src);
+        return launch_fp8<1>(d, st, x, topk_idx, slot, recv, recv_scale, recv_src);
     }
-    return launch_status();
+    switch (lane_tasks(d.H / 8)) {
+        case 8: return launch_bf16<8>(d, st, x, topk_idx, slot, recv, recv_src);
+        case 7: return launch_bf16<7>(d, st, x, topk_idx, slot, recv, recv_src);
+        case 2: return launch_bf16<2>(d, st, x, topk_idx, slot, recv, recv_src);
+        case 1: return launch_bf16<1>(d, st, x, topk_idx, slot, recv, recv_src);
+        default: return launch_bf16<4>(d, st, x, topk_idx, slot, recv, recv_src);
+    }
 }

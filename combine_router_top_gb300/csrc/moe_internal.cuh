@@ -11,6 +11,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <initializer_list>
+
 #include "moe.h"
 
 namespace moe {
@@ -55,7 +57,29 @@ inline int persistent_grid(long long units, int resident, int max_blocks) {
     return g < 1 ? 1 : (int)g;
 }
 
+// Tasks per lane per work unit: the largest of 8, 7, 4, 2, 1 for which units of
+// 32*U tasks tile a row of n_tasks exactly (else 4).
+inline int lane_tasks(int n_tasks) {
+    for (int u : {8, 7, 4, 2, 1})
+        if (n_tasks % (32 * u) == 0) return u;
+    return 4;
+}
+
 // ---- device helpers -------------------------------------------------------
+
+// Walks the work units unit0, unit0 + stride, ... of a (row, segment) grid
+// with `segs` segments per row, keeping (row, seg) without any division in
+// the loop.
+struct UnitWalk {
+    unsigned row, seg, drow, dseg, segs;
+    __device__ __forceinline__ UnitWalk(unsigned unit0, unsigned stride, unsigned segs_)
+        : row(unit0 / segs_), seg(unit0 % segs_), drow(stride / segs_), dseg(stride % segs_), segs(segs_) {}
+    __device__ __forceinline__ void next() {
+        row += drow;
+        seg += dseg;
+        if (seg >= segs) { seg -= segs; row += 1; }
+    }
+};
 
 // 16-byte load through the read-only path, not kept in L1 (each row is read
 // once). Only for data no kernel writes while this one runs.
