@@ -135,24 +135,21 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ top
         for (int i = 0; i < U; ++i) {
             const uint32_t wv[8] = {a[2 * i].x, a[2 * i].y, a[2 * i].z, a[2 * i].w,
                                     a[2 * i + 1].x, a[2 * i + 1].y, a[2 * i + 1].z, a[2 * i + 1].w};
-            float f[16];
+            // |x| max of the 16 values on packed bf16 pairs (exact), then over the 8 lanes
+            uint32_t m = 0;
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
-                f[2 * h] = bf16_lo(wv[h]);
-                f[2 * h + 1] = bf16_hi(wv[h]);
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int h = 0; h < 16; ++h) amax = fmaxf(amax, fabsf(f[h]));
+            for (int h = 0; h < 8; ++h) m = bf16x2_absmax(m, wv[h]);
+            float amax = fmaxf(bf16_lo(m), bf16_hi(m));
             amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
             amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
-            const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+            const float sc = e4m3_block_scale(amax);
             uint32_t q[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const uint32_t lo = pack_e4m3x2(__fdiv_rn(f[4 * h], sc), __fdiv_rn(f[4 * h + 1], sc));
-                const uint32_t hi = pack_e4m3x2(__fdiv_rn(f[4 * h + 2], sc), __fdiv_rn(f[4 * h + 3], sc));
+                const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc));
+                const uint32_t hi =
+                    pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc));
                 q[h] = lo | (hi << 16);
             }
             qv[i] = make_uint4(q[0], q[1], q[2], q[3]);

@@ -100,6 +100,13 @@ __device__ __forceinline__ void st_v4(void *p, uint4 v) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Elementwise max of |a| and |b| on bf16 pairs (exact: no rounding involved).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    const __nv_bfloat162 r = __hmax2(__habs2(*reinterpret_cast<const __nv_bfloat162 *>(&a)),
+                                     __habs2(*reinterpret_cast<const __nv_bfloat162 *>(&b)));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // Two floats -> bf16 pair, round to nearest even (lo in the low half).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -110,6 +117,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
     __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
     return static_cast<uint32_t>(s);
+}
+
+// Block scale of the fp8 dispatch: amax / 448 in fp32 (IEEE division), 1 for
+// an all-zero block.
+__device__ __forceinline__ float e4m3_block_scale(float amax) {
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
 // Total order on fp32 logits as unsigned keys: larger logit -> larger key,

@@ -216,3 +216,4 @@ def test_dbo_small_and_odd_batches(T):
     if T == 1:
         assert int(to_host(bufs[0]["counts"]).sum()) == 0
     ctx.close()
+
