@@ -1,0 +1,54 @@
+"""Multi-rank plumbing of bench.py, on CPU with the gloo backend and two
+ranks: the max-over-ranks timing and the barrier that bracket the replicas'
+timed region (N GPUs run N independent replicas of the step)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    try:
+        bench.barrier(world)
+        mx = bench.reduce_max(1.5 + rank, world)
+        # the slowest rank's dispatch+combine time sets the whole-job rate
+        dc_ms = bench.reduce_max(0.040 if rank == 0 else 0.050, world)
+        q.put((rank, mx, world * 1024 / (dc_ms * 1e-3)))
+        bench.barrier(world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_max_and_barrier():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert [g[1] for g in got] == [2.5, 2.5]
+    assert all(abs(g[2] - 2 * 1024 / 50e-6) < 1e-3 for g in got)
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.reduce_max(3.25, 1) == 3.25
+    bench.barrier(1)
