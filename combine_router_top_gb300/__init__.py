@@ -66,6 +66,7 @@ def lib() -> C.CDLL:
             "moe_validate": ([pp], i),
             "moe_route_workspace_bytes": ([pp], C.c_size_t),
             "moe_route": ([pp, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
+            "moe_route_noalloc": ([pp, P, P, P, P, P, P, P, P, P], i),
             "moe_dispatch": ([pp, P, P, P, P, P, P, P], i),
             "moe_expert_synthetic": ([pp, P, P, P, P, P, P], i),
             "moe_combine": ([pp, P, P, P, P, P, P], i),
@@ -81,7 +82,8 @@ def lib() -> C.CDLL:
     return _lib
 
 
-EXPORTS = ("moe_status_string", "moe_validate", "moe_route_workspace_bytes", "moe_route", "moe_dispatch",
+EXPORTS = ("moe_status_string", "moe_validate", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
+           "moe_dispatch",
            "moe_expert_synthetic", "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing")
 
 
@@ -130,6 +132,14 @@ def moe_route(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_counts, d
                          _ptr(slot), _ptr(rank_counts), _ptr(dropped), _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check("moe_route", rc)
+
+
+def moe_route_noalloc(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_counts, dropped, stream=None):
+    """moe_route with the library's own static scratch instead of a workspace
+    (for callers that cannot allocate device memory)."""
+    rc = lib().moe_route_noalloc(C.byref(p), _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+                                 _ptr(offsets), _ptr(slot), _ptr(rank_counts), _ptr(dropped), _stream(stream))
+    _check("moe_route_noalloc", rc)
 
 
 def moe_dispatch(p, x, topk_idx, slot, recv, recv_scale, recv_src, stream=None):

@@ -18,6 +18,8 @@
 //      sum of the earlier tiles' counts; slot = base + rank in tile, or -1 at
 //      or past the capacity. The last CTA also forms the totals, offsets,
 //      rank counts and drops.
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -220,4 +222,54 @@ extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *top
     route_finalize_kernel<<<n_tiles > 0 ? n_tiles : 1, 1024, 0, st>>>(d.T, n_tiles, d.E, d.k, d.R, d.C, wc, topk_idx,
                                                                      slot, counts, offsets, rank_counts, dropped);
     return launch_status();
+}
+
+// ---- allocation-free variant ---------------------------------------------
+//
+// Some callers cannot call cudaMalloc at all: code that runs while a stream is
+// being captured into a CUDA graph (allocation is not allowed then), runtimes
+// that forbid device allocation after start-up, and plugin interfaces that hand
+// a kernel only its input and output buffers. For them moe_route_noalloc keeps
+// the route workspace in a file-scope device array instead of a caller buffer.
+
+namespace {
+
+constexpr size_t kStaticRouteScratchBytes = 1u << 20;     // 1 MiB on every GPU that loads the library
+constexpr int kMaxScratchDevices = 64;
+
+__device__ __align__(256) unsigned char g_route_scratch[kStaticRouteScratchBytes];
+
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of g_route_scratch on the current device, looked up once per
+// device (the host-side name of the array is not a device address).
+int route_scratch_address(void **addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_route_noalloc(const moe_problem *p, const float *logits, int32_t *topk_idx, float *topk_w,
+                                 int32_t *counts, int32_t *offsets, int32_t *slot, int32_t *rank_counts,
+                                 int32_t *dropped, void *stream) {
+    using namespace moe;
+    const int rc = check_problem(p, nullptr);
+    if (rc != MOE_OK) return rc;
+    if (moe_route_workspace_bytes(p) > kStaticRouteScratchBytes) return MOE_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    const int ac = route_scratch_address(&scratch);
+    if (ac != MOE_OK) return ac;
+    return moe_route(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_counts, dropped, scratch,
+                     kStaticRouteScratchBytes, stream);
 }

@@ -122,6 +122,31 @@ int moe_route(const moe_problem *p, const float *logits,
               int32_t *rank_counts, int32_t *dropped,
               void *workspace, size_t workspace_bytes, void *stream);
 
+/* moe_route without a workspace argument, for callers that cannot allocate
+ * device memory: code running while a stream is captured into a CUDA graph
+ * (cudaMalloc is not allowed during capture), runtimes that forbid device
+ * allocation once started, and plugin interfaces that pass a kernel only its
+ * inputs and outputs. The paper (the pages cited above) has no counterpart of
+ * this call; it computes exactly what moe_route computes, on the same kernels.
+ *  Scratch: a 1 MiB array in device memory, defined in the library, which
+ *  every GPU that loads the library holds until the process exits. The call
+ *  returns MOE_ERR_UNSUPPORTED, launching nothing, when the problem needs more
+ *  (moe_route_workspace_bytes(p) > 1 MiB: 32 tokens x E experts x 4 bytes per
+ *  tile of 32 tokens; for instance more than 32768 tokens at E = 256).
+ *  Set-up: the first call on a device looks up the array's device address
+ *  with that device current (cudaGetSymbolAddress); make that first call
+ *  before any stream capture on the device. Later calls do no CUDA call other
+ *  than the kernel launches.
+ *  Sharing: all calls on a device use the same array, which keeps the last
+ *  call's contents (the route kernels overwrite what they read, so nothing
+ *  needs clearing). Calls whose executions overlap on the GPU (other streams,
+ *  other threads) race on the array: order them on one stream.
+ *  Arguments, outputs and errors are otherwise those of moe_route. */
+int moe_route_noalloc(const moe_problem *p, const float *logits,
+                      int32_t *topk_idx, float *topk_w,
+                      int32_t *counts, int32_t *offsets, int32_t *slot,
+                      int32_t *rank_counts, int32_t *dropped, void *stream);
+
 /* Step 3: dispatch. [PMC §Dispatch]: rows are placed into one tensor for the
  * downstream grouped GEMM, all tokens of one expert grouped together whatever
  * their source, and each row's origin is stored so that combine can send it
