@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kBlock, KMAX <= 8 ? 4 : 2)
 combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ topk_idx,
                const float *__restrict__ topk_w, const int32_t *__restrict__ slot,
                uint4 *__restrict__ out, int T, int H8, int k, int C, int segs) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     UnitWalk wk(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs);
     if (wk.row >= (unsigned)T) return;                         // warp-uniform
@@ -161,6 +162,7 @@ expert_bf16_kernel(const uint4 *__restrict__ recv, const int32_t *__restrict__ c
                    const float *__restrict__ s, uint4 *__restrict__ y, int E, int C, int H8, int segs) {
     __shared__ int32_t off[kMaxExperts + 1];
     __shared__ int32_t warp_tot[32];
+    pdl_enter();
     kept_row_offsets(counts, E, C, off, warp_tot);
     const int lane = threadIdx.x & 31;
     const unsigned rows = off[E];
@@ -205,6 +207,7 @@ expert_fp8_kernel(const uint4 *__restrict__ recv_q, const float *__restrict__ re
                   uint4 *__restrict__ y, int E, int C, int H, int segs) {
     __shared__ int32_t off[kMaxExperts + 1];
     __shared__ int32_t warp_tot[32];
+    pdl_enter();
     kept_row_offsets(counts, E, C, off, warp_tot);
     const int lane = threadIdx.x & 31;
     const unsigned n_tasks = H / 16, nb = H / 128, rows = off[E];
@@ -251,9 +254,10 @@ int launch_expert_fp8(const Dims &d, long long max_rows, cudaStream_t st, const 
     const long long units = max_rows * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-    expert_fp8_kernel<U><<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(recv), scale, counts, s,
-                                                  static_cast<uint4 *>(y), d.E, d.C, d.H, segs);
-    return launch_status();
+    if (launch_pdl(expert_fp8_kernel<U>, grid, kBlock, st, static_cast<const uint4 *>(recv), scale, counts, s,
+                   static_cast<uint4 *>(y), d.E, d.C, d.H, segs) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 template <int U>
@@ -264,9 +268,10 @@ int launch_expert_bf16(const Dims &d, long long max_rows, cudaStream_t st, const
     const long long units = max_rows * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-    expert_bf16_kernel<U><<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(recv), counts, s,
-                                                   static_cast<uint4 *>(y), d.E, d.C, d.H / 8, segs);
-    return launch_status();
+    if (launch_pdl(expert_bf16_kernel<U>, grid, kBlock, st, static_cast<const uint4 *>(recv), counts, s,
+                   static_cast<uint4 *>(y), d.E, d.C, d.H / 8, segs) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 }  // namespace
@@ -317,8 +322,10 @@ int launch_combine(const moe::Dims &d, cudaStream_t st, const uint4 *y, const in
     const long long units = (long long)d.T * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-    combine_kernel<KMAX><<<grid, kBlock, 0, st>>>(y, idx, w, slot, out, d.T, H8, d.k, d.C, segs);
-    return launch_status();
+    if (launch_pdl(combine_kernel<KMAX>, grid, kBlock, st, y, idx, w, slot, out, d.T, H8, d.k, d.C, segs) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 }  // namespace
 

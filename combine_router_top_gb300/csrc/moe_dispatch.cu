@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kBlock)
 dispatch_bf16_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
                      const int32_t *__restrict__ slot, uint4 *__restrict__ recv,
                      int32_t *__restrict__ recv_src, int T, int H8, int k, int C, int segs) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     UnitWalk w(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs);
     if (w.row >= (unsigned)T) return;                                  // warp-uniform
@@ -112,6 +113,7 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ top
                     const int32_t *__restrict__ slot, uint4 *__restrict__ recv_q,
                     float *__restrict__ recv_scale, int32_t *__restrict__ recv_src, int T, int H,
                     int k, int C, int segs) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const unsigned n_tasks = H / 16, nb = H / 128;
     UnitWalk w(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs);
@@ -189,10 +191,10 @@ int launch_fp8(const Dims &d, cudaStream_t st, const void *x, const int32_t *idx
     const long long units = (long long)d.T * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-    dispatch_fp8_kernel<U><<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(x), idx, slot,
-                                                    static_cast<uint4 *>(recv), scale, src, d.T, d.H, d.k, d.C,
-                                                    segs);
-    return launch_status();
+    if (launch_pdl(dispatch_fp8_kernel<U>, grid, kBlock, st, static_cast<const uint4 *>(x), idx, slot,
+                   static_cast<uint4 *>(recv), scale, src, d.T, d.H, d.k, d.C, segs) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 template <int U>
@@ -204,9 +206,10 @@ int launch_bf16(const Dims &d, cudaStream_t st, const void *x, const int32_t *id
     const long long units = (long long)d.T * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-    dispatch_bf16_kernel<U><<<grid, kBlock, 0, st>>>(static_cast<const uint4 *>(x), idx, slot,
-                                                     static_cast<uint4 *>(recv), src, d.T, H8, d.k, d.C, segs);
-    return launch_status();
+    if (launch_pdl(dispatch_bf16_kernel<U>, grid, kBlock, st, static_cast<const uint4 *>(x), idx, slot,
+                   static_cast<uint4 *>(recv), src, d.T, H8, d.k, d.C, segs) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 }  // namespace

@@ -65,7 +65,35 @@ inline int lane_tasks(int n_tasks) {
     return 4;
 }
 
+// Launches `kernel` on `st` allowing programmatic dependent launch: the grid
+// may be scheduled while the previous kernel on the stream finishes. Every
+// kernel of this library starts with pdl_wait(), so none touches global memory
+// before its predecessor has completed and flushed.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), int grid, int block, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 // ---- device helpers -------------------------------------------------------
+
+// Programmatic dependent launch: wait until the previous grid on the stream
+// has completed and its memory is visible, then let the next grid launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_launch_dependents();
+}
 
 // Walks the work units unit0, unit0 + stride, ... of a (row, segment) grid
 // with `segs` segments per row, keeping (row, seg) without any division in
