@@ -50,7 +50,7 @@ UNIT = "tokens/s"
 WORKLOAD = "dsv3_fp8"
 DTYPE = "e4m3+bf16 (fp32 arithmetic)"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 4          # route, dispatch, expert, combine: one launch each
+KERNELS_PER_STEP = 5          # route (top-k/tile, finalize), dispatch, expert, combine
 CPU_SAMPLE_TOKENS = 256       # the oracle's bounded sample: 2 of the 8 source ranks
 
 

@@ -230,8 +230,7 @@ def alloc_buffers(p: moe_problem, device="cuda") -> dict:
         "recv_scale": torch.empty((E, Cap, H // 128), **f32) if fp8 else None,
         "recv_src": torch.empty((E, Cap), **i32),
         "y": torch.empty((E, Cap, H), dtype=torch.int16, device=device),
-        # zeroed: the route ticket counter in its first bytes must start at 0
-        "workspace": torch.zeros(ws, dtype=torch.uint8, device=device),
+        "workspace": torch.empty(ws, dtype=torch.uint8, device=device),
     }
     return b
 

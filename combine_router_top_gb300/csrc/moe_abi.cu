@@ -59,11 +59,10 @@ int moe_validate(const moe_problem *p) { return moe::check_problem(p, nullptr); 
 size_t moe_route_workspace_bytes(const moe_problem *p) {
     moe::Dims d;
     if (moe::check_problem(p, &d) != MOE_OK) return 0;
-    size_t tiles = ((size_t)d.T + moe::kTileTokens - 1) / moe::kTileTokens;
-    if (tiles == 0) tiles = 1;
-    // [ticket counter, 16 bytes][per-tile counts]
-    const size_t bytes = 16 + tiles * (size_t)d.E * sizeof(int32_t);
-    return (bytes + 255) & ~(size_t)255;
+    const size_t tiles = ((size_t)d.T + moe::kTileTokens - 1) / moe::kTileTokens;
+    size_t bytes = tiles * (size_t)d.E * sizeof(int32_t);
+    bytes = (bytes + 255) & ~(size_t)255;
+    return bytes < 256 ? 256 : bytes;
 }
 
 }  // extern "C"

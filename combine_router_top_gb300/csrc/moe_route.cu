@@ -7,22 +7,18 @@
 // tokens per destination expert. [PMC §Portable kernels]: a fixed per-expert
 // bound lets every sender compute a unique destination address.
 //
-// One launch, no atomic that decides an order, no waiting:
-//   Every CTA takes a tile of 32 tokens, one warp per token. Top-k by k rounds
-//   of a warp arg-max (redux.sync max on an order-preserving 32-bit key,
-//   ballot for the lowest tied lane). Weights by expf and one IEEE division.
-//   Each chosen expert sets the token's bit in a per-expert 32-bit shared-
-//   memory mask: a pair's rank within the tile is the popcount of the lower
-//   bits, the tile's count per expert the popcount. The CTA writes its counts,
-//   fences, and takes a ticket (atomicInc, which wraps back to 0 on the last
-//   one). The CTA that draws the last ticket sees every tile's counts: it
-//   scans them per expert over the tiles (tile bases), writes every pair's
-//   slot = base + rank (or -1 at or past C), and the totals, offsets, rank
-//   counts and drops.
-//
-// Workspace: [ticket counter, 16 bytes][tile counts: max(tiles,1) x E int32].
-// The counter must be zero before the first call; every call that completes
-// leaves it zero.
+// Two launches (the second a programmatic dependent of the first, so its
+// launch latency hides behind the first), no atomics that decide an order:
+//   K1 route_topk_tile: one CTA per tile of 32 tokens, one warp per token.
+//      Top-k by k rounds of a warp arg-max (redux.sync max on an order-
+//      preserving 32-bit key, ballot for the lowest tied lane). Weights by
+//      expf and one IEEE division. Each chosen expert sets the token's bit in
+//      a per-expert 32-bit shared-memory mask; a pair's rank within the tile is
+//      the popcount of the lower bits, the tile's count per expert the popcount.
+//   K2 route_finalize: one CTA per tile. The tile's per-expert base is the
+//      sum of the earlier tiles' counts; slot = base + rank in tile, or -1 at
+//      or past the capacity. The last CTA also forms the totals, offsets,
+//      rank counts and drops.
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -33,23 +29,17 @@ namespace {
 // Lane l of a token's warp owns experts [l*V, l*V + V) (clipped to E).
 template <int V>
 __global__ void __launch_bounds__(1024, 1)
-route_kernel(const float *__restrict__ logits, int T, int E, int k, int R, int C, int n_tiles,
-             int32_t *__restrict__ topk_idx, float *__restrict__ topk_w, int32_t *__restrict__ slot,
-             unsigned *__restrict__ ticket, int32_t *__restrict__ tile_counts, int32_t *__restrict__ counts,
-             int32_t *__restrict__ offsets, int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped) {
+route_topk_tile_kernel(const float *__restrict__ logits, int T, int E, int k,
+                       int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+                       int32_t *__restrict__ slot_rank, int32_t *__restrict__ tile_counts) {
     __shared__ uint32_t mask[kMaxExperts];
-    __shared__ int32_t part[1024];
-    __shared__ int32_t racc[kMaxExperts];
-    __shared__ int32_t warp_sums[32];
-    __shared__ int32_t dacc;
-    __shared__ unsigned s_ticket;
     pdl_enter();
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int wt = tid >> 5;                          // token within the tile
+    const int lane = threadIdx.x & 31;
+    const int wt = threadIdx.x >> 5;                 // token within the tile
     const int tile = blockIdx.x;
     const int t = tile * kTileTokens + wt;
-    const bool active = t < T;                        // warp-uniform
-    for (int e = tid; e < E; e += blockDim.x) mask[e] = 0u;
+    const bool active = t < T;                       // warp-uniform
+    for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0u;
     __syncthreads();
 
     int my_e = 0;
@@ -106,61 +96,66 @@ route_kernel(const float *__restrict__ logits, int T, int E, int k, int R, int C
     }
     __syncthreads();
     if (active && lane < k)
-        slot[(size_t)t * k + lane] = __popc(mask[my_e] & ((1u << wt) - 1u));   // rank within the tile
-    for (int e = tid; e < E; e += blockDim.x) tile_counts[(size_t)tile * E + e] = __popc(mask[e]);
+        slot_rank[(size_t)t * k + lane] = __popc(mask[my_e] & ((1u << wt) - 1u));
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        tile_counts[(size_t)tile * E + e] = __popc(mask[e]);
+}
 
-    // the last CTA to finish finalises every tile
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_ticket = atomicInc(ticket, (unsigned)gridDim.x - 1u);
-    __syncthreads();
-    if (s_ticket != gridDim.x - 1u) return;           // block-uniform
-    __threadfence();
-
-    // exclusive scan over tiles per expert; 1024/E thread groups split the tiles
+// CTA b finalises tile b: its per-expert base is the sum of the counts of
+// tiles 0..b-1 (read from the workspace; 1024/E thread groups split the
+// tiles), slot = base + rank in tile (or -1 at or past C). The last CTA also
+// adds its own tile to get the totals and writes counts, offsets,
+// rank_counts and dropped.
+__global__ void __launch_bounds__(1024, 1)
+route_finalize_kernel(int T, int n_tiles, int E, int k, int R, int C, const int32_t *__restrict__ tile_counts,
+                      const int32_t *__restrict__ topk_idx, int32_t *__restrict__ slot,
+                      int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                      int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped) {
+    __shared__ int32_t part[1024];
+    __shared__ int32_t base[kMaxExperts];
+    __shared__ int32_t racc[kMaxExperts];
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t dacc;
+    pdl_enter();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x;
+    const bool last = b == (int)gridDim.x - 1;
     const int G = (1024 / E) > 0 ? (1024 / E) : 1;
     const int g = tid / E, e = tid % E;
-    const int per = (n_tiles + G - 1) / G;
-    const int b0 = min(n_tiles, g * per), b1 = min(n_tiles, b0 + per);
     if (g < G) {
-        int sum = 0;
+        int s = 0;
 #pragma unroll 8
-        for (int b = b0; b < b1; ++b) sum += __ldcg(tile_counts + (size_t)b * E + e);
-        part[tid] = sum;
+        for (int tt = g; tt < b; tt += G) s += __ldg(tile_counts + (size_t)tt * E + e);
+        part[tid] = s;
     }
-    for (int i = tid; i < E; i += blockDim.x) racc[i] = 0;
-    if (tid == 0) dacc = 0;
+    if (last) {
+        for (int i = tid; i < E; i += blockDim.x) racc[i] = 0;
+        if (tid == 0) dacc = 0;
+    }
     __syncthreads();
-    int v = 0;                                         // total of expert tid (tid < E)
-    if (g < G) {
-        int run = 0;
-        for (int gg = 0; gg < g; ++gg) run += part[gg * E + e];
-        for (int b = b0; b < b1; ++b) {
-            const int c = __ldcg(tile_counts + (size_t)b * E + e);
-            tile_counts[(size_t)b * E + e] = run;       // becomes the tile's base for expert e
-            run += c;
-        }
+    if (tid < E) {
+        int s = 0;
+        for (int gg = 0; gg < G; ++gg) s += part[gg * E + tid];
+        base[tid] = s;
     }
-    if (tid < E)
-        for (int gg = 0; gg < G; ++gg) v += part[gg * E + tid];
-    __syncthreads();                                   // bases visible to the whole CTA
-
-    // slots of every pair
-    const int n_pairs = T * k;
+    __syncthreads();
+    const int t0 = b * kTileTokens;
+    const int n_pairs = (min(T - t0, kTileTokens) > 0 ? min(T - t0, kTileTokens) : 0) * k;
     for (int i = tid; i < n_pairs; i += blockDim.x) {
-        const int b = (i / k) / kTileTokens;
-        const int sl = __ldcg(tile_counts + (size_t)b * E + __ldcg(topk_idx + i)) + __ldcg(slot + i);
-        slot[i] = sl < C ? sl : -1;
+        const size_t gi = (size_t)t0 * k + i;
+        const int s = base[__ldg(topk_idx + gi)] + slot[gi];
+        slot[gi] = s < C ? s : -1;
     }
+    if (!last) return;                                   // block-uniform
 
-    // offsets = exclusive scan of the totals over experts
+    // totals = base of this (last) tile + its own counts
+    const int v = tid < E ? base[tid] + (b < n_tiles ? __ldg(tile_counts + (size_t)b * E + tid) : 0) : 0;
     int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(kFull, incl, o);
         if (lane >= o) incl += n;
     }
-    const int warp = tid >> 5;
     if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
     if (warp == 0) {
@@ -187,15 +182,9 @@ route_kernel(const float *__restrict__ logits, int T, int E, int k, int R, int C
 }
 
 template <int V>
-int launch_route(int grid, cudaStream_t st, const float *logits, const Dims &d, int n_tiles, int32_t *idx,
-                 float *w, int32_t *slot, void *workspace, int32_t *counts, int32_t *offsets, int32_t *rank_counts,
-                 int32_t *dropped) {
-    unsigned *ticket = static_cast<unsigned *>(workspace);
-    int32_t *tile_counts = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + 16);
-    if (launch_pdl(route_kernel<V>, grid, 1024, st, logits, d.T, d.E, d.k, d.R, d.C, n_tiles, idx, w, slot,
-                   ticket, tile_counts, counts, offsets, rank_counts, dropped) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    return MOE_OK;
+cudaError_t launch_topk(int n_tiles, cudaStream_t st, const float *logits, const Dims &d, int32_t *idx,
+                        float *w, int32_t *slot, int32_t *wc) {
+    return launch_pdl(route_topk_tile_kernel<V>, n_tiles, 1024, st, logits, d.T, d.E, d.k, idx, w, slot, wc);
 }
 
 }  // namespace
@@ -221,18 +210,27 @@ extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *top
         return MOE_ERR_INVALID_ARG;
 
     cudaStream_t st = as_stream(stream);
+    int32_t *wc = static_cast<int32_t *>(workspace);
     const int n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
-    // an empty batch still runs one block: it writes the zero counts
-    const int grid = n_tiles > 0 ? n_tiles : 1;
-    const int per_lane = (d.E + 31) / 32;
-    int rc2;
-    if (per_lane <= 1) rc2 = launch_route<1>(grid, st, logits, d, n_tiles, topk_idx, topk_w, slot, workspace, counts, offsets, rank_counts, dropped);
-    else if (per_lane <= 2) rc2 = launch_route<2>(grid, st, logits, d, n_tiles, topk_idx, topk_w, slot, workspace, counts, offsets, rank_counts, dropped);
-    else if (per_lane <= 4) rc2 = launch_route<4>(grid, st, logits, d, n_tiles, topk_idx, topk_w, slot, workspace, counts, offsets, rank_counts, dropped);
-    else if (per_lane <= 8) rc2 = launch_route<8>(grid, st, logits, d, n_tiles, topk_idx, topk_w, slot, workspace, counts, offsets, rank_counts, dropped);
-    else if (per_lane <= 16) rc2 = launch_route<16>(grid, st, logits, d, n_tiles, topk_idx, topk_w, slot, workspace, counts, offsets, rank_counts, dropped);
-    else rc2 = launch_route<32>(grid, st, logits, d, n_tiles, topk_idx, topk_w, slot, workspace, counts, offsets, rank_counts, dropped);
-    return rc2;
+    if (n_tiles > 0) {
+        const int per_lane = (d.E + 31) / 32;
+        cudaError_t e;
+        if (per_lane <= 1) e = launch_topk<1>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else if (per_lane <= 2) e = launch_topk<2>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else if (per_lane <= 4) e = launch_topk<4>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else if (per_lane <= 8) e = launch_topk<8>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else if (per_lane <= 16) e = launch_topk<16>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        else e = launch_topk<32>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    // an empty batch still runs one finalise block: it writes the zero counts.
+    // Launched as a programmatic dependent of the top-k kernel: its launch
+    // latency overlaps the top-k kernel's run.
+    if (launch_pdl(route_finalize_kernel, n_tiles > 0 ? n_tiles : 1, 1024, st, d.T, n_tiles, d.E, d.k, d.R, d.C,
+                   static_cast<const int32_t *>(wc), static_cast<const int32_t *>(topk_idx), slot, counts, offsets,
+                   rank_counts, dropped) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 // ---- allocation-free variant ---------------------------------------------

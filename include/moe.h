@@ -89,12 +89,8 @@ const char *moe_status_string(int status);
 int moe_validate(const moe_problem *p);
 
 /* Bytes of device workspace moe_route needs for this problem (host-only, no
- * CUDA call); 0 if the problem is invalid. The workspace holds a 16-byte
- * ticket counter followed by one 32-bit count per (tile of 32 tokens,
- * expert). The counter (its first 16 bytes) must be zero before the
- * workspace's first use, e.g. allocate it zero-filled; every moe_route call
- * that completes leaves it zero, so a workspace can be reused for any
- * problem. After a failed or aborted launch, zero it again. */
+ * CUDA call); 0 if the problem is invalid. The workspace holds one 32-bit
+ * count per (tile of 32 tokens, expert). Its contents need no initialisation. */
 size_t moe_route_workspace_bytes(const moe_problem *p);
 
 /* Step 1 and 2: router top-k with renormalised softmax weights, then the
@@ -119,9 +115,7 @@ size_t moe_route_workspace_bytes(const moe_problem *p);
  *  Results are deterministic and independent of the launch configuration.
  *  NaN logits give unspecified (but in-range) indices.
  *  workspace: device scratch of at least moe_route_workspace_bytes(p) bytes,
- *  16-byte aligned, zero-filled before its first use (see above), not shared
- *  with a concurrent call. One kernel launch; the block that finishes last
- *  (ticket counter) scans the tiles' counts, so nothing ever waits. */
+ *  16-byte aligned, not shared with a concurrent call. */
 int moe_route(const moe_problem *p, const float *logits,
               int32_t *topk_idx, float *topk_w,
               int32_t *counts, int32_t *offsets, int32_t *slot,

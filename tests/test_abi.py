@@ -82,9 +82,9 @@ def test_validate_accepts_workloads(moe):
 
 
 def test_route_workspace_bytes(moe):
-    p = mk(moe)        # 16-byte ticket + 1024 tokens -> 32 tiles of 32 x 256 experts x int32, 256-rounded
-    assert moe.moe_route_workspace_bytes(p) == (16 + 32 * 256 * 4 + 255) // 256 * 256
-    assert moe.moe_route_workspace_bytes(mk(moe, T=0)) == (16 + 256 * 4 + 255) // 256 * 256
+    p = mk(moe)        # 1024 tokens -> 32 tiles of 32, 256 experts, int32
+    assert moe.moe_route_workspace_bytes(p) == 32 * 256 * 4
+    assert moe.moe_route_workspace_bytes(mk(moe, T=0)) == 256
     assert moe.moe_route_workspace_bytes(mk(moe, T=33, E=8, R=2)) % 256 == 0
 
 
