@@ -20,6 +20,7 @@ MOE_ERR_INVALID_ARG = -1
 MOE_ERR_UNSUPPORTED = -2
 MOE_ERR_CUDA = -3
 MOE_ERR_DEVICE_CHECK = -4
+MOE_ERR_TIMEOUT = -5
 
 MOE_DTYPE_BF16 = 0
 MOE_DTYPE_FP8_E4M3_B128 = 1
@@ -64,6 +65,7 @@ def lib() -> C.CDLL:
         sig = {
             "moe_status_string": ([i], C.c_char_p),
             "moe_validate": ([pp], i),
+            "moe_device_status": ([], i),
             "moe_route_workspace_bytes": ([pp], C.c_size_t),
             "moe_route": ([pp, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
             "moe_route_noalloc": ([pp, P, P, P, P, P, P, P, P, P], i),
@@ -82,7 +84,7 @@ def lib() -> C.CDLL:
     return _lib
 
 
-EXPORTS = ("moe_status_string", "moe_validate", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
+EXPORTS = ("moe_status_string", "moe_validate", "moe_device_status", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
            "moe_dispatch",
            "moe_expert_synthetic", "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing")
 
@@ -117,6 +119,11 @@ def _stream(stream):
 def _check(fn, rc):
     if rc != MOE_OK:
         raise MoeError(fn, rc)
+
+
+def moe_device_status() -> int:
+    """MOE_OK, or MOE_ERR_TIMEOUT if a bounded device wait gave up since the last call (synchronises)."""
+    return lib().moe_device_status()
 
 
 def moe_validate(p: moe_problem) -> int:

@@ -2,7 +2,27 @@
 // Host code only; nothing here touches the GPU except the cached SM count.
 #include "moe_internal.cuh"
 
+#include <mutex>
+
 namespace moe {
+
+namespace {
+__device__ unsigned g_device_status;    // kStatus* bits, set by kernels whose bounded waits gave up
+std::mutex g_status_mutex;
+unsigned *g_status_addr[64] = {};
+}  // namespace
+
+unsigned *device_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (g_status_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<unsigned *>(p);
+    }
+    return g_status_addr[dev];
+}
 
 int check_problem(const moe_problem *p, Dims *d) {
     if (p == nullptr) return MOE_ERR_INVALID_ARG;
@@ -50,11 +70,23 @@ const char *moe_status_string(int status) {
         case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: request outside what this build supports";
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA: the CUDA runtime reported an error";
         case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK: a device-side consistency check failed";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait gave up";
         default: return "unknown moe_status";
     }
 }
 
 int moe_validate(const moe_problem *p) { return moe::check_problem(p, nullptr); }
+
+int moe_device_status(void) {
+    unsigned *w = moe::device_status_word();
+    if (w == nullptr) return MOE_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (v == 0) return MOE_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    return (v & moe::kStatusWaitGaveUp) ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_CHECK;
+}
 
 size_t moe_route_workspace_bytes(const moe_problem *p) {
     moe::Dims d;

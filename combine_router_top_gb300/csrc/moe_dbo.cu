@@ -73,11 +73,12 @@ extern "C" int dbo_step(moe_dbo_ctx *ctx, const moe_problem *full, const void *x
     moe_problem p[2] = {*full, *full};
     p[0].num_tokens = T0;
     p[1].num_tokens = T1;
-    // overlapped pair: at most four 128-thread blocks per SM each, so that both fit
+    // overlapped pair: combine(0) keeps two 256-thread blocks per SM (half the
+    // register file), dispatch(1) up to eight small bulk-copy blocks per SM, so
+    // that both have blocks resident at the same time
     moe_problem p_overlap[2] = {p[0], p[1]};
-    const int cap = full->max_blocks > 0 ? full->max_blocks : 4 * sm_count();
-    p_overlap[0].max_blocks = cap;
-    p_overlap[1].max_blocks = cap;
+    p_overlap[0].max_blocks = full->max_blocks > 0 ? full->max_blocks : 2 * sm_count();
+    p_overlap[1].max_blocks = full->max_blocks > 0 ? full->max_blocks : 8 * sm_count();
 
     const size_t xrow = (size_t)d.H * 2, lrow = (size_t)d.E * sizeof(float);
     const void *x_ub[2] = {x, d.T ? byte_ptr(x, xrow * T0) : nullptr};

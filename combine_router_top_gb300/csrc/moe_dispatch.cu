@@ -16,6 +16,8 @@
 // shuffle (ascending j). The next unit's routing and row data are loaded
 // before the current unit is stored, so that two units' loads are in flight.
 // recv_src is written on a token's first segment.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -182,6 +184,146 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ top
     }
 }
 
+// ---- TMA (bulk-copy) dispatch ----------------------------------------------
+//
+// fp8: a CTA of 64 threads takes a unit (token, 1024-element segment): one
+// bulk copy brings the 2 KB of bf16 into shared memory (mbarrier), each
+// thread quantises 16 elements into a shared-memory code row and the 8 scales,
+// and one thread issues, for every kept destination, a 1 KB bulk store of the
+// codes and a 32-byte bulk store of the scales. bf16: a warp takes a token:
+// one bulk copy of the row in, one bulk store per destination out (each lane
+// j < k stores its own destination), no per-element instruction at all.
+// Both loop grid-stride over their units when max_blocks caps the grid.
+
+constexpr int kTmaSeg = 1024;                    // fp8 unit: elements
+constexpr int kTmaFp8Threads = kTmaSeg / 16;     // one 16-element task per thread
+constexpr int kTmaBf16MaxRowBytes = 32768;       // bf16 rows staged whole (H <= 16384)
+
+__global__ void __launch_bounds__(kTmaFp8Threads)
+dispatch_fp8_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
+                        const int32_t *__restrict__ slot, uint8_t *__restrict__ recv_q,
+                        float *__restrict__ recv_scale, int32_t *__restrict__ recv_src, int T, int H, int k,
+                        int C, unsigned *status) {
+    __shared__ __align__(128) uint4 xs[kTmaSeg * 2 / 16];
+    __shared__ __align__(128) uint4 qs[kTmaSeg / 16];
+    __shared__ __align__(16) float ss[kTmaSeg / 128];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_row[kMaxTopK];
+    __shared__ int s_n;
+    pdl_enter();
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int segs = H / kTmaSeg, nb = H / 128;
+    const long long units = (long long)T * segs;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    unsigned phase = 0;
+    for (long long u = blockIdx.x; u < units; u += gridDim.x, phase ^= 1u) {
+        const int t = (int)(u / segs), seg = (int)(u % segs);
+        if (tid == 0) {
+            fence_proxy_async_smem();                // earlier generic reads of xs before the bulk write
+            mbar_expect_tx(&bar, kTmaSeg * 2);
+            bulk_g2s(xs, x + (size_t)t * H + (size_t)seg * kTmaSeg, kTmaSeg * 2, &bar);
+        }
+        if (tid < 32) {
+            const int dest = load_dest(t, k, C, topk_idx, slot);
+            const unsigned kept = __ballot_sync(kFull, dest >= 0);
+            if (dest >= 0) {
+                s_row[__popc(kept & ((1u << lane) - 1u))] = dest;
+                if (seg == 0) recv_src[dest] = t;
+            }
+            if (lane == 0) s_n = __popc(kept);
+        }
+        const bool ok = mbar_wait_bounded(&bar, phase);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                atomicOr(status, kStatusWaitGaveUp);
+                mbar_wait_bounded(&bar, phase);          // the load in flight, bounded again
+                bulk_wait_all();
+            }
+            return;
+        }
+        // quantise the 16 elements of task tid (lanes 8g .. 8g+7 share a 128-element block)
+        const uint4 a = xs[2 * tid], c = xs[2 * tid + 1];
+        const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+        uint32_t m = 0;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) m = bf16x2_absmax(m, wv[h]);
+        float amax = fmaxf(bf16_lo(m), bf16_hi(m));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+        const float sc = e4m3_block_scale(amax);
+        uint32_t q[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc));
+            const uint32_t hi =
+                pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc));
+            q[h] = lo | (hi << 16);
+        }
+        qs[tid] = make_uint4(q[0], q[1], q[2], q[3]);
+        if ((tid & 7) == 0) ss[tid >> 3] = sc;
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            const int nd = s_n;
+            for (int j = 0; j < nd; ++j) {
+                const size_t row = (size_t)s_row[j];
+                bulk_s2g(recv_q + row * H + (size_t)seg * kTmaSeg, qs, kTmaSeg);
+                bulk_s2g(recv_scale + row * nb + (size_t)seg * (kTmaSeg / 128), ss, (kTmaSeg / 128) * 4);
+            }
+            bulk_commit();
+            bulk_wait_read_all();            // the codes and scales may be overwritten after this
+        }
+        __syncthreads();
+    }
+    if (tid == 0) bulk_wait_all();           // every store complete before the grid ends
+}
+
+__global__ void __launch_bounds__(32)
+dispatch_bf16_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
+                         const int32_t *__restrict__ slot, uint16_t *__restrict__ recv,
+                         int32_t *__restrict__ recv_src, int T, int H, int k, int C, unsigned *status) {
+    extern __shared__ __align__(128) unsigned char rowbuf[];
+    __shared__ __align__(8) uint64_t bar;
+    pdl_enter();
+    const int lane = threadIdx.x;
+    const unsigned bytes = (unsigned)H * 2u;
+    if (lane == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    unsigned phase = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x, phase ^= 1u) {
+        if (lane == 0) {
+            mbar_expect_tx(&bar, bytes);
+            bulk_g2s(rowbuf, x + (size_t)t * H, bytes, &bar);
+        }
+        const int dest = load_dest(t, k, C, topk_idx, slot);
+        if (dest >= 0) recv_src[dest] = t;
+        const bool ok = mbar_wait_bounded(&bar, phase);
+        if (!__all_sync(kFull, ok)) {
+            if (lane == 0) {
+                atomicOr(status, kStatusWaitGaveUp);
+                mbar_wait_bounded(&bar, phase);
+            }
+            bulk_wait_all();
+            return;
+        }
+        if (dest >= 0) {                     // lane j stores the row to its own destination
+            bulk_s2g(recv + (size_t)dest * H, rowbuf, bytes);
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+        __syncwarp();
+    }
+    bulk_wait_all();                         // every store complete before the grid ends
+}
+
 template <int U>
 int launch_fp8(const Dims &d, cudaStream_t st, const void *x, const int32_t *idx, const int32_t *slot, void *recv,
                float *scale, int32_t *src) {
@@ -231,6 +373,28 @@ extern "C" int moe_dispatch(const moe_problem *p, const void *x, const int32_t *
         return MOE_ERR_INVALID_ARG;
 
     cudaStream_t st = as_stream(stream);
+    unsigned *status = device_status_word();
+    if (status == nullptr) return MOE_ERR_CUDA;
+    if (fp8 && d.H % kTmaSeg == 0) {
+        static int resident = resident_blocks(dispatch_fp8_tma_kernel, kTmaFp8Threads);
+        const long long units = (long long)d.T * (d.H / kTmaSeg);
+        const int grid = d.max_blocks > 0 ? persistent_grid(units, resident, d.max_blocks)
+                                          : (int)std::min<long long>(units, 1LL << 30);
+        if (launch_pdl(dispatch_fp8_tma_kernel, grid, kTmaFp8Threads, st, static_cast<const uint16_t *>(x), topk_idx,
+                       slot, static_cast<uint8_t *>(recv), recv_scale, recv_src, d.T, d.H, d.k, d.C, status) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (!fp8 && d.H * 2 <= kTmaBf16MaxRowBytes) {
+        const size_t smem = (size_t)d.H * 2;
+        const int grid = d.max_blocks > 0 ? std::min(d.T, d.max_blocks) : d.T;
+        if (launch_pdl_smem(dispatch_bf16_tma_kernel, grid, 32, smem, st, static_cast<const uint16_t *>(x), topk_idx,
+                            slot, static_cast<uint16_t *>(recv), recv_src, d.T, d.H, d.k, d.C, status) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     if (fp8) {
         // two tasks per lane per unit: 64 tasks = 1024 elements; the next unit's rows are prefetched
         const int n_tasks = d.H / 16;

@@ -56,7 +56,8 @@ typedef enum moe_status {
     MOE_ERR_INVALID_ARG = -1,   /* a size, pointer or alignment check failed       */
     MOE_ERR_UNSUPPORTED = -2,   /* valid request outside what this build supports  */
     MOE_ERR_CUDA = -3,          /* the CUDA runtime reported an error               */
-    MOE_ERR_DEVICE_CHECK = -4   /* a device-side consistency check failed           */
+    MOE_ERR_DEVICE_CHECK = -4,  /* a device-side consistency check failed           */
+    MOE_ERR_TIMEOUT = -5        /* a bounded device wait gave up (moe_device_status)  */
 } moe_status;
 
 typedef enum moe_dispatch_dtype {
@@ -83,6 +84,15 @@ typedef struct moe_problem {
 
 /* Human-readable name of a moe_status value. Never NULL; static storage. */
 const char *moe_status_string(int status);
+
+/* Device status of this library on the current device. Kernels that wait
+ * on their own asynchronous copies (mbarrier waits on bulk loads) bound every
+ * wait; a wait that gives up records it in a status word on the device, drains
+ * what it still has in flight and returns, leaving its outputs incomplete.
+ * This call synchronises with the device (a blocking copy: keep it out of
+ * timed or captured regions), returns MOE_ERR_TIMEOUT if such a wait gave up
+ * since the last call, MOE_OK otherwise, and clears the word. */
+int moe_device_status(void);
 
 /* Host-only validation of a problem (no CUDA call). Returns MOE_OK or
  * MOE_ERR_INVALID_ARG. */

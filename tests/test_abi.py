@@ -48,7 +48,7 @@ def test_library_does_not_export_cuda_runtime(moe):
 
 
 def test_status_strings(moe):
-    for s in [0, -1, -2, -3, -4]:
+    for s in [0, -1, -2, -3, -4, -5]:
         assert moe.moe_status_string(s).startswith("MOE_")
     assert moe.moe_status_string(12345) == "unknown moe_status"
 
