@@ -12,9 +12,9 @@
 // Schedule (compute = caller's compute stream, comm = caller's comm stream):
 //   compute: route(0) route(1) dispatch(0) expert(0) [E0] combine(0) wait(D1) expert(1) combine(1)
 //   comm:    wait(entry) ........................ wait(E0) dispatch(1) [D1]
-// so dispatch of micro-batch 1 runs while micro-batch 0 combines. The two
-// overlapped kernels get a capped grid (grid-stride loops) so that both have
-// thread blocks resident at the same time.
+// so dispatch of micro-batch 1 runs while micro-batch 0 combines. Combine(0)
+// gets a capped grid (grid-stride loop) so that dispatch(1)'s blocks find
+// room on every SM at the same time.
 #include <new>
 
 #include "moe_internal.cuh"
@@ -74,11 +74,11 @@ extern "C" int dbo_step(moe_dbo_ctx *ctx, const moe_problem *full, const void *x
     p[0].num_tokens = T0;
     p[1].num_tokens = T1;
     // overlapped pair: combine(0) keeps two 256-thread blocks per SM (half the
-    // register file), dispatch(1) up to eight small bulk-copy blocks per SM, so
-    // that both have blocks resident at the same time
+    // register file); dispatch(1), whose bulk-copy blocks are small and
+    // short-lived, is not capped: its blocks fill what combine leaves free
     moe_problem p_overlap[2] = {p[0], p[1]};
     p_overlap[0].max_blocks = full->max_blocks > 0 ? full->max_blocks : 2 * sm_count();
-    p_overlap[1].max_blocks = full->max_blocks > 0 ? full->max_blocks : 8 * sm_count();
+    p_overlap[1].max_blocks = full->max_blocks;
 
     const size_t xrow = (size_t)d.H * 2, lrow = (size_t)d.E * sizeof(float);
     const void *x_ub[2] = {x, d.T ? byte_ptr(x, xrow * T0) : nullptr};
