@@ -40,6 +40,7 @@ def lib():
             "oracle_dispatch_fp8": [i32, i32, i32, i32, i32, P, P, P, P, P, P],
             "oracle_expert_synthetic": [i32, i32, i32, i32, P, P, P, P, P],
             "oracle_combine": [i32, i32, i32, i32, i32, P, P, P, P, P],
+            "oracle_scale_rows": [i64, P, C.c_float, P],
         }.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -210,3 +211,34 @@ def run_dbo(x, logits, s, k: int, R: int, Cap: int, fp8: bool) -> dict:
         parts.append(r)
         outs.append(r["out"])
     return {"out": np.concatenate(outs, axis=0), "parts": parts}
+
+
+def scale_rows(x: np.ndarray, a: float) -> np.ndarray:
+    """bf16(float(x) * a), the stand-in for the layer compute around the MoE block."""
+    xb = np.ascontiguousarray(x, dtype=np.uint16)
+    out = np.empty_like(xb)
+    _check(lib().oracle_scale_rows(xb.size, _p(xb), float(np.float32(a)), _p(out)), "oracle_scale_rows")
+    return out
+
+
+def run_dbo_layers(x, logits_layers, s, k: int, R: int, Cap: int, alpha: float, sigma: float) -> dict:
+    """Layers of the dual-batch-overlap schedule, micro-batch by micro-batch.
+    [DBO §Introduction]: per layer and micro-batch u, A0 (here h = bf16(x a)),
+    A1 (the MoE gate: route on the layer's logits), dispatch of h, the experts,
+    S (shared expert: bf16(h s)) and combine, whose output is the next layer's
+    input. Returns the last layer's output and shared-expert output."""
+    L, T, E = logits_layers.shape
+    H = x.shape[1]
+    out = np.empty((T, H), dtype=np.uint16)
+    shared = np.empty((T, H), dtype=np.uint16)
+    for (a, b) in micro_batches(T):
+        if b == a:
+            continue
+        xu = np.ascontiguousarray(x[a:b])
+        for l in range(L):
+            h = scale_rows(xu, alpha)
+            r = run_path(h, logits_layers[l, a:b], s, k, R, Cap, False)
+            shared[a:b] = scale_rows(h, sigma)
+            xu = r["out"]
+        out[a:b] = xu
+    return {"out": out, "shared": shared}

@@ -404,3 +404,18 @@ int oracle_combine(int32_t T, int32_t H, int32_t E, int32_t k, int32_t C,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Stand-in for the layer compute around the MoE block in the dual-batch-    */
+/* overlap schedule ([DBO §Introduction]: A0 = qkv projection, A1 = core      */
+/* attention + out projection + MoE gate, S = shared expert):                */
+/*   out[i] = bf16(float(in[i]) * a)   (fp32 product, round to nearest even). */
+/* ------------------------------------------------------------------------ */
+int oracle_scale_rows(int64_t n, const uint16_t *in, float a, uint16_t *out)
+{
+    if (n < 0)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = bf16_encode_rne(bf16_decode(in[i]) * a);
+    return 0;
+}

@@ -385,3 +385,38 @@ def test_dbo_output_is_the_two_halves_in_order(inputs_of):
     # combine is per-token, so the single-shot output matches too
     full = O.run_path(d["x"], d["logits"], d["s"], w.k, w.R, w.C, False)
     assert np.array_equal(r["out"], full["out"])
+
+
+# ---- layers of the dual-batch-overlap schedule ------------------------------------
+
+def test_scale_rows_is_exact_for_powers_of_two_and_rounds_otherwise(inputs_of):
+    x = inputs_of("tiny")["x"]
+    assert np.array_equal(bf16_vals(O.scale_rows(x, 2.0)), 2 * bf16_vals(x))
+    assert np.array_equal(O.scale_rows(x, 1.0), x)
+    y = bf16_vals(O.scale_rows(x, 1.1)).astype(np.float64)
+    exact = bf16_vals(x).astype(np.float64) * np.float64(np.float32(1.1))
+    assert np.all(np.abs(y - exact) <= np.abs(exact) * 2.0 ** -8)
+
+
+def test_dbo_layers_one_layer_reduces_to_the_path(inputs_of):
+    """With one layer and alpha = 1 the layer is exactly the MoE path of its
+    micro-batches; the shared-expert output is bf16(x sigma)."""
+    w = W.WORKLOADS["v2lite"]
+    d = inputs_of("v2lite")
+    r = O.run_dbo_layers(d["x"], d["logits"][None], d["s"], w.k, w.R, w.C, 1.0, 0.5)
+    ref = O.run_dbo(d["x"], d["logits"], d["s"], w.k, w.R, w.C, False)
+    assert np.array_equal(r["out"], ref["out"])
+    assert np.array_equal(bf16_vals(r["shared"]), 0.5 * bf16_vals(d["x"]))
+
+
+def test_dbo_layers_closed_form_two_layers():
+    """Two layers with unit expert scales: each layer multiplies a token by
+    alpha * sum_j w_j (= alpha, no drops) up to rounding: out ~ alpha^2 x."""
+    rng = np.random.default_rng(9)
+    T, H, E, k = 64, 256, 8, 2
+    x = bf16_bits(rng.standard_normal((T, H)))
+    lg = rng.standard_normal((2, T, E)).astype(np.float32)
+    r = O.run_dbo_layers(x, lg, np.ones(E, np.float32), k, 2, T, 0.5, 1.0)
+    xf = bf16_vals(x).astype(np.float64)
+    got = bf16_vals(r["out"]).astype(np.float64)
+    assert np.all(np.abs(got - 0.25 * xf) <= np.abs(0.25 * xf) * 4 * 2.0 ** -8 + 1e-30)
