@@ -493,6 +493,54 @@ def run_dbo(args, dev) -> dict:
             "reps": reps, "l2": "flushed before every step"}
 
 
+def run_dbo_layers(args, dev, layers: int = 4, busy_fmas: int = 256) -> dict:
+    """The [DBO] layer schedule on the 8192-token workload: two streams eager,
+    two streams replayed from a CUDA graph, and the same work on one stream."""
+    import torch
+    import combine_router_top_gb300 as M
+    w = W.WORKLOADS["dbo"]
+    T1 = w.T - w.T // 2
+    pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C)
+    x = torch.from_numpy(W.make_x(w).view(np.int16)).to(dev)
+    lg = torch.from_numpy(np.stack([W.make_logits(w.with_(seed=w.seed + 31 * l)) for l in range(layers)])).to(dev)
+    s = torch.from_numpy(W.expert_scale(w)).to(dev)
+    bufs = [M.alloc_buffers(M.problem(T1, w.H, w.E, w.k, w.R, w.C), dev) for _ in range(2)]
+    h, shared, out = (torch.empty((w.T, w.H), dtype=torch.int16, device=dev) for _ in range(3))
+    a = M.dbo_layers_args(pf, layers, x, lg, s, bufs, h, shared, out, 0.75, 1.5, busy_fmas)
+    comp, comm = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ctx = M.dbo_create()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    fw = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    fr = torch.ones_like(fw)
+
+    def timed(launch, reps=8):
+        ts = []
+        with torch.cuda.stream(comp):
+            for i in range(2 + reps):
+                fw.fill_(1)
+                fr.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(comp)
+                launch()
+                e1.record(comp)
+                e1.synchronize()
+                if i >= 2:
+                    ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    comp.wait_stream(torch.cuda.current_stream())
+    two = timed(lambda: M.dbo_layers(ctx, a, comp, comm))
+    one = timed(lambda: M.dbo_layers(ctx, a, comp, comp))
+    M.dbo_layers_capture(ctx, a, comp, comm)
+    graph = timed(lambda: M.dbo_graph_launch(ctx, comp))
+    ctx.close()
+    return {"workload": f"dbo layers: {layers} layers, T={w.T} split {w.T // 2}/{T1}, H={w.H}, E={w.E}, "
+                        f"top_k={w.k}, C={w.C}, bf16; A0/S stand-ins with {busy_fmas} busy FMAs per 8 elements",
+            "ms_per_layer_two_streams": two / layers, "ms_per_layer_graph": graph / layers,
+            "ms_per_layer_one_stream": one / layers, "speedup_vs_one_stream": one / two,
+            "l2": "flushed before every run of the layers"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -510,6 +558,7 @@ def main():
     if rank == 0:
         if world == 1 and not args.no_dbo:
             line["dbo"] = run_dbo(args, dev)
+            line["dbo_layers"] = run_dbo_layers(args, dev)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(W.WORKLOADS[WORKLOAD])
         print(json.dumps(line), flush=True)

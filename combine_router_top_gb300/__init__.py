@@ -44,6 +44,12 @@ class moe_dbo_timing(C.Structure):
                                          "overlap_fraction")]
 
 
+class moe_dbo_layers_args(C.Structure):
+    _fields_ = [("full", moe_problem), ("n_layers", C.c_int32), ("busy_fmas", C.c_int32), ("alpha", C.c_float),
+                ("sigma", C.c_float), ("x", C.c_void_p), ("logits", C.c_void_p), ("s", C.c_void_p),
+                ("bufs", moe_ubatch_bufs * 2), ("h", C.c_void_p), ("shared", C.c_void_p), ("out", C.c_void_p)]
+
+
 class MoeError(RuntimeError):
     def __init__(self, fn: str, status: int):
         super().__init__(f"{fn} failed: {moe_status_string(status)} ({status})")
@@ -76,6 +82,10 @@ def lib() -> C.CDLL:
             "dbo_destroy": ([P], None),
             "dbo_step": ([P, pp, P, P, P, C.POINTER(moe_ubatch_bufs), P, P, P, i], i),
             "dbo_read_timing": ([P, C.POINTER(moe_dbo_timing)], i),
+            "moe_layer_stand_in": ([P, P, C.c_int64, C.c_float, C.c_int32, P], i),
+            "dbo_layers": ([P, C.POINTER(moe_dbo_layers_args), P, P], i),
+            "dbo_layers_capture": ([P, C.POINTER(moe_dbo_layers_args), P, P], i),
+            "dbo_graph_launch": ([P, P], i),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -86,7 +96,8 @@ def lib() -> C.CDLL:
 
 EXPORTS = ("moe_status_string", "moe_validate", "moe_device_status", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
            "moe_dispatch",
-           "moe_expert_synthetic", "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing")
+           "moe_expert_synthetic", "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
+           "moe_layer_stand_in", "dbo_layers", "dbo_layers_capture", "dbo_graph_launch")
 
 
 def moe_status_string(status: int) -> str:
@@ -249,3 +260,33 @@ def run_path(p: moe_problem, x, logits, s, bufs: dict, out, stream=None):
     moe_dispatch(p, x, bufs["topk_idx"], bufs["slot"], bufs["recv"], bufs.get("recv_scale"), bufs["recv_src"], stream)
     moe_expert_synthetic(p, bufs["recv"], bufs.get("recv_scale"), bufs["counts"], s, bufs["y"], stream)
     moe_combine(p, bufs["y"], bufs["topk_idx"], bufs["topk_w"], bufs["slot"], out, stream)
+
+
+def moe_layer_stand_in(x, out, a: float, busy_fmas: int = 0, stream=None):
+    """out = bf16(x * a) (+ busy work that does not change the output)."""
+    _check("moe_layer_stand_in", lib().moe_layer_stand_in(_ptr(x), _ptr(out), x.numel(), float(a), int(busy_fmas),
+                                                          _stream(stream)))
+
+
+def dbo_layers_args(p_full, n_layers, x, logits, s, bufs2, h, shared, out, alpha=1.0, sigma=1.0, busy_fmas=0):
+    """moe_dbo_layers_args from tensors (the struct keeps raw pointers: keep the tensors alive)."""
+    a = moe_dbo_layers_args()
+    a.full = p_full
+    a.n_layers, a.busy_fmas, a.alpha, a.sigma = int(n_layers), int(busy_fmas), float(alpha), float(sigma)
+    a.x, a.logits, a.s = _ptr(x), _ptr(logits), _ptr(s)
+    a.bufs[0], a.bufs[1] = ubatch_bufs(bufs2[0]), ubatch_bufs(bufs2[1])
+    a.h, a.shared, a.out = _ptr(h), _ptr(shared), _ptr(out)
+    return a
+
+
+def dbo_layers(ctx: DboContext, args, compute_stream, comm_stream):
+    _check("dbo_layers", lib().dbo_layers(ctx.handle, C.byref(args), _stream(compute_stream), _stream(comm_stream)))
+
+
+def dbo_layers_capture(ctx: DboContext, args, compute_stream, comm_stream):
+    _check("dbo_layers_capture", lib().dbo_layers_capture(ctx.handle, C.byref(args), _stream(compute_stream),
+                                                          _stream(comm_stream)))
+
+
+def dbo_graph_launch(ctx: DboContext, stream=None):
+    _check("dbo_graph_launch", lib().dbo_graph_launch(ctx.handle, _stream(stream)))

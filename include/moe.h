@@ -253,6 +253,62 @@ int dbo_step(moe_dbo_ctx *ctx, const moe_problem *full,
  * synchronisation: call it outside a timed or captured region) and fills *t. */
 int dbo_read_timing(moe_dbo_ctx *ctx, moe_dbo_timing *t /* host */);
 
+/* ---- Dual batch overlap over layers ------------------------------------- */
+
+/* Stand-in for the layer compute around the MoE block (the qkv projection,
+ * the core attention and out projection, and the shared expert of [DBO
+ * §Introduction]'s schedule, whose weights are out of scope):
+ *   out[i] = bf16(float(in[i]) * a)   (fp32 product, round to nearest even),
+ * over n_elements bf16 values (a multiple of 8; in and out 16-byte aligned,
+ * not overlapping), plus busy_fmas (0 .. 2^20) dependent fp32 FMAs of busy
+ * work per 8 elements that do not change the output: a tunable compute cost
+ * standing in for the GEMMs. */
+int moe_layer_stand_in(const void *in, void *out, int64_t n_elements, float a,
+                       int32_t busy_fmas, void *stream);
+
+/* Arguments of dbo_layers. Micro-batch u of T = full.num_tokens tokens is
+ * rows [0, T/2) (u = 0) or [T/2, T) (u = 1); bufs[u] is sized for T - T/2
+ * tokens (as for dbo_step). full.dispatch_dtype must be MOE_DTYPE_BF16. */
+typedef struct moe_dbo_layers_args {
+    moe_problem full;         /* T = both micro-batches                               */
+    int32_t n_layers;         /* L >= 1                                               */
+    int32_t busy_fmas;        /* busy work of the A0 and S stand-ins                  */
+    float alpha;              /* A0 stand-in: h = bf16(x * alpha)                      */
+    float sigma;              /* S stand-in: shared = bf16(h * sigma)                  */
+    const void *x;            /* [T][H] bf16: input of layer 0                         */
+    const float *logits;      /* [L][T][E] f32: router logits of every layer           */
+    const float *s;           /* [E] f32: synthetic expert scales                      */
+    moe_ubatch_bufs bufs[2];  /* per micro-batch route / dispatch / expert buffers    */
+    void *h;                  /* [T][H] bf16 scratch: A0 output, dispatched rows      */
+    void *shared;             /* [T][H] bf16: S output of the last layer             */
+    void *out;                /* [T][H] bf16: layer activations; layer L's output    */
+} moe_dbo_layers_args;
+
+/* L layers of the [DBO §Introduction] schedule on two streams of one GPU.
+ * Per layer l and micro-batch u: A0 (h = bf16(x_u * alpha), x_u the layer's
+ * input), A1 (moe_route on logits[l]), D (moe_dispatch of h), MLP
+ * (moe_expert_synthetic), S (shared = bf16(h * sigma)) and C (moe_combine,
+ * whose output is the next layer's input). A0, A1, MLP and S run on
+ * `compute`, D and C on `comm`, enqueued in the page's order:
+ *   D_1 | A0_0 A1_0 | D_0 | MLP_1 | C_1 | S_1 | MLP_0 | C_0 | S_0 | A0_1 A1_1 (next layer)
+ * with each receive as an event wait; a prologue runs layer 0's A0_1 A1_1.
+ * `comm` first waits for the work already on `compute`; at return every step
+ * is ordered before later work on `compute`. With compute == comm the same
+ * work runs in the same order on one stream (the no-overlap baseline). No
+ * host synchronisation, no allocation: the call can be captured into a CUDA
+ * graph (dbo_layers_capture). */
+int dbo_layers(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *compute_stream, void *comm_stream);
+
+/* Captures dbo_layers(ctx, a, compute, comm) into a CUDA graph owned by ctx
+ * (relaxed stream capture; `compute` must not be the legacy default stream),
+ * replacing any graph captured before. Make one eager call with the same
+ * shapes first: first calls look up device properties. The graph keeps the
+ * pointers of `a`. */
+int dbo_layers_capture(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *compute_stream, void *comm_stream);
+
+/* Launches the graph last captured by dbo_layers_capture on `stream`. */
+int dbo_graph_launch(moe_dbo_ctx *ctx, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

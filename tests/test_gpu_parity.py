@@ -217,3 +217,109 @@ def test_dbo_small_and_odd_batches(T):
         assert int(to_host(bufs[0]["counts"]).sum()) == 0
     ctx.close()
 
+
+
+def _layers_setup(w, L, alpha, sigma, busy=0):
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev
+    rng = np.random.default_rng(w.seed)
+    x = W.make_x(w)
+    lg = np.stack([W.make_logits(w.with_(seed=w.seed + 31 * l)) for l in range(L)])
+    s = W.expert_scale(w)
+    T1 = w.T - w.T // 2
+    pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C)
+    bufs = [M.alloc_buffers(M.problem(T1, w.H, w.E, w.k, w.R, w.C), "cuda:0") for _ in range(2)]
+    t = {"x": to_dev(x), "lg": to_dev(lg), "s": to_dev(s),
+         "h": torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0"),
+         "shared": torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0"),
+         "out": torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0")}
+    args = M.dbo_layers_args(pf, L, t["x"], t["lg"], t["s"], bufs, t["h"], t["shared"], t["out"], alpha, sigma, busy)
+    return x, lg, s, t, bufs, args
+
+
+def _layers_sequential(w, L, alpha, sigma, t):
+    """The same kernels, micro-batch after micro-batch and layer after layer, on one stream."""
+    import torch
+    import combine_router_top_gb300 as M
+    out = torch.empty_like(t["out"])
+    shared = torch.empty_like(t["out"])
+    for (a, b) in [(0, w.T // 2), (w.T // 2, w.T)]:
+        if b == a:
+            continue
+        p = M.problem(b - a, w.H, w.E, w.k, w.R, w.C)
+        bb = M.alloc_buffers(p, "cuda:0")
+        xu = t["x"][a:b].clone()
+        h = torch.empty_like(xu)
+        for l in range(L):
+            M.moe_layer_stand_in(xu, h, alpha)
+            M.run_path(p, h, t["lg"][l, a:b].contiguous(), t["s"], bb, xu)
+            M.moe_layer_stand_in(h, shared[a:b], sigma)
+        out[a:b] = xu
+    torch.cuda.synchronize()
+    return out, shared
+
+
+@pytest.mark.parametrize("name,L,busy", [("tiny", 3, 0), ("v2lite", 2, 64), ("mixtral_skew", 2, 0)])
+def test_dbo_layers_match_sequential_and_oracle(name, L, busy):
+    """[DBO §Introduction] schedule over L layers on two streams: bit-identical
+    to the same kernels run one after another on one stream, and within L+1
+    bf16 ulps of the oracle (the routing is identical, each layer's combine is
+    within 1 ulp)."""
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_host, ulp_distance
+    w = W.WORKLOADS[name]
+    alpha, sigma = 0.75, 1.5
+    x, lg, s, t, bufs, args = _layers_setup(w, L, alpha, sigma, busy)
+    comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    comp.wait_stream(torch.cuda.current_stream())
+    ctx = M.dbo_create()
+    M.dbo_layers(ctx, args, comp, comm)
+    torch.cuda.synchronize()
+    got, got_sh = to_host(t["out"], np.uint16), to_host(t["shared"], np.uint16)
+    ref, ref_sh = _layers_sequential(w, L, alpha, sigma, t)
+    assert np.array_equal(got, to_host(ref, np.uint16))
+    assert np.array_equal(got_sh, to_host(ref_sh, np.uint16))
+    o = O.run_dbo_layers(x, lg, s, w.k, w.R, w.C, alpha, sigma)
+    assert ulp_distance(got, o["out"]).max() <= L + 1
+    assert ulp_distance(got_sh, o["shared"]).max() <= L + 1
+    ctx.close()
+
+
+def test_dbo_layers_graph_replay_equals_eager():
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_host
+    w = W.WORKLOADS["v2lite"]
+    x, lg, s, t, bufs, args = _layers_setup(w, 3, 0.5, 2.0, 16)
+    comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    comp.wait_stream(torch.cuda.current_stream())
+    ctx = M.dbo_create()
+    M.dbo_layers(ctx, args, comp, comm)                 # eager first
+    torch.cuda.synchronize()
+    eager = to_host(t["out"], np.uint16).copy()
+    eager_sh = to_host(t["shared"], np.uint16).copy()
+    M.dbo_layers_capture(ctx, args, comp, comm)
+    for _ in range(2):
+        t["out"].fill_(0)
+        t["shared"].fill_(0)
+        torch.cuda.synchronize()
+        M.dbo_graph_launch(ctx, comp)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_host(t["out"], np.uint16), eager)
+        assert np.array_equal(to_host(t["shared"], np.uint16), eager_sh)
+    ctx.close()
+
+
+def test_layer_stand_in_is_exact():
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev, to_host
+    w = W.WORKLOADS["tiny"]
+    x = W.make_x(w)
+    out = torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0")
+    for a, busy in [(1.1, 0), (0.3, 100)]:
+        M.moe_layer_stand_in(to_dev(x), out, a, busy)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_host(out, np.uint16), O.scale_rows(x, a))
