@@ -196,8 +196,16 @@ extern "C" int dbo_layers(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *
     moe_problem p[2] = {a->full, a->full};
     p[0].num_tokens = T0;
     p[1].num_tokens = T1;
-    moe_problem pc[2] = {p[0], p[1]};                     // combine on the comm stream keeps half the SMs
-    pc[0].max_blocks = pc[1].max_blocks = a->full.max_blocks > 0 ? a->full.max_blocks : 2 * sm_count();
+    // combine (comm stream) keeps at most two 256-thread blocks per SM so that
+    // compute-stream blocks find room beside it; the compute-stream kernels run
+    // full waves (capping them as well was measured slower: each kernel loses
+    // more throughput than the overlap wins back) and dispatch's small
+    // bulk-copy blocks fill what is left
+    const int cap = a->full.max_blocks > 0 ? a->full.max_blocks : 2 * sm_count();
+    moe_problem pc[2] = {p[0], p[1]};
+    pc[0].max_blocks = pc[1].max_blocks = cap;
+    moe_problem pe[2] = {p[0], p[1]};
+    const int compute_cap = a->full.max_blocks;
 
     const size_t rowb = (size_t)d.H * 2;
     auto rows = [&](const void *base, int u) { return static_cast<const char *>(base) + rowb * row0[u]; };
@@ -220,7 +228,7 @@ extern "C" int dbo_layers(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *
     auto attention = [&](int l, int u) -> int {
         const void *in = l == 0 ? rows(a->x, u) : rows(a->out, u);
         const moe_ubatch_bufs &b = a->bufs[u];
-        int r = moe_layer_stand_in(in, rows_w(a->h, u), (int64_t)Tu[u] * d.H, a->alpha, a->busy_fmas, compute_stream);
+        int r = layer_stand_in(in, rows_w(a->h, u), (int64_t)Tu[u] * d.H, a->alpha, a->busy_fmas, compute_cap, cs);
         if (r != MOE_OK) return r;
         r = moe_route(&p[u], logits(l, u), b.topk_idx, b.topk_w, b.counts, b.offsets, b.slot, b.rank_counts,
                       b.dropped, b.workspace, b.workspace_bytes, compute_stream);
@@ -238,7 +246,7 @@ extern "C" int dbo_layers(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *
     auto experts = [&](int u) -> int {                     // compute stream, after this micro-batch's dispatch
         const moe_ubatch_bufs &b = a->bufs[u];
         if (cudaStreamWaitEvent(cs, ctx->d[u], 0) != cudaSuccess) return MOE_ERR_CUDA;
-        const int r = moe_expert_synthetic(&p[u], b.recv, b.recv_scale, b.counts, a->s, b.y, compute_stream);
+        const int r = moe_expert_synthetic(&pe[u], b.recv, b.recv_scale, b.counts, a->s, b.y, compute_stream);
         if (r != MOE_OK) return r;
         return cudaEventRecord(ctx->mlp[u], cs) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     };
@@ -250,8 +258,8 @@ extern "C" int dbo_layers(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *
         return cudaEventRecord(ctx->c[u], ms) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     };
     auto shared_expert = [&](int u) -> int {               // compute stream
-        return moe_layer_stand_in(rows(a->h, u), rows_w(a->shared, u), (int64_t)Tu[u] * d.H, a->sigma,
-                                  a->busy_fmas, compute_stream);
+        return layer_stand_in(rows(a->h, u), rows_w(a->shared, u), (int64_t)Tu[u] * d.H, a->sigma, a->busy_fmas,
+                              compute_cap, cs);
     };
 
     MOE_CUDA(cudaEventRecord(ctx->entry, cs));

@@ -40,6 +40,9 @@ unsigned *device_status_word();
 constexpr unsigned kStatusWaitGaveUp = 1u;     // a bounded wait on a copy gave up
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 int sm_count();                         // SMs of the current device (cached)
+// moe_layer_stand_in with a cap on its grid (moe_layers.cu).
+int layer_stand_in(const void *in, void *out, int64_t n_elements, float a, int32_t busy_fmas, int max_blocks,
+                   cudaStream_t st);
 inline int launch_status(void) {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
