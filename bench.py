@@ -16,7 +16,9 @@ by CUDA events on its stream and the flush is outside the brackets.
   pipelined    the four calls back to back, flushed once per step (the two
                timed loops each run K steps: gpu_launches counts both).
   e2e          the same path through the public API with pinned host buffers:
-               H2D of x and logits, the four calls, D2H of out, per step.
+               H2D of x and logits, the four calls, D2H of out, every step;
+               double-buffered so that neighbouring steps' copies overlap the
+               compute (the serial figure is reported beside it).
   roofline     the combine kernel (the larger of the two kernels the metric
                names): algorithmic bytes / mean duration vs measured HBM peak.
   cpu_baseline the CPU oracle, single-threaded, on a bounded sample.
@@ -378,32 +380,70 @@ def run_ours(args, rank: int, world: int, local: int):
     step_ms_max = reduce_max(step_ms, world, dev)
     comb_ms = reduce_max(ms["combine"], world, dev)
 
-    # end to end through the public API: pinned host in, pinned host out
-    xp = torch.from_numpy(x_h.view(np.int16)).pin_memory()
-    lp = torch.from_numpy(lg_h).pin_memory()
-    op = torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()
-    x2, lg2, out2 = torch.empty_like(x), torch.empty_like(lg), torch.empty_like(out)
+    # end to end through the public API: pinned host in, pinned host out, every
+    # step. Serial: copy in, the four calls, copy out, one after another.
+    # Pipelined (a serving loop): two buffer sets; step i+1's inputs are copied
+    # in and step i-1's output copied out while step i computes.
+    sets = []
+    for _ in range(2):
+        sets.append({"x": torch.empty_like(x), "lg": torch.empty_like(lg), "out": torch.empty_like(out),
+                     "b": M.alloc_buffers(p, dev),
+                     "xp": torch.from_numpy(x_h.view(np.int16)).pin_memory(),
+                     "lp": torch.from_numpy(lg_h).pin_memory(),
+                     "op": torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()})
+    s_in, s_comp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
 
-    def e2e_step():
-        x2.copy_(xp, non_blocking=True)
-        lg2.copy_(lp, non_blocking=True)
-        M.run_path(p, x2, lg2, s, b, out2, stream)
-        op.copy_(out2, non_blocking=True)
+    def e2e_serial_step(z):
+        z["x"].copy_(z["xp"], non_blocking=True)
+        z["lg"].copy_(z["lp"], non_blocking=True)
+        M.run_path(p, z["x"], z["lg"], s, z["b"], z["out"], stream)
+        z["op"].copy_(z["out"], non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
+    def e2e_run(n, pipelined):
+        ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("in", "comp", "out")}
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world, dev)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        if not pipelined:
+            for i in range(n):
+                e2e_serial_step(sets[0])
+            e1.record(stream)
+        else:
+            for st_ in (s_in, s_comp, s_out):
+                st_.wait_stream(stream)
+            for i in range(n):
+                z, j = sets[i % 2], i % 2
+                if i >= 2:
+                    s_in.wait_event(ev["comp"][j])          # set j's previous step has read its inputs
+                with torch.cuda.stream(s_in):
+                    z["x"].copy_(z["xp"], non_blocking=True)
+                    z["lg"].copy_(z["lp"], non_blocking=True)
+                ev["in"][j].record(s_in)
+                s_comp.wait_event(ev["in"][j])
+                if i >= 2:
+                    s_comp.wait_event(ev["out"][j])         # set j's previous output has been copied out
+                M.run_path(p, z["x"], z["lg"], s, z["b"], z["out"], s_comp)
+                ev["comp"][j].record(s_comp)
+                s_out.wait_event(ev["comp"][j])
+                with torch.cuda.stream(s_out):
+                    z["op"].copy_(z["out"], non_blocking=True)
+                ev["out"][j].record(s_out)
+            stream.wait_stream(s_out)
+            stream.wait_stream(s_comp)
+            stream.wait_stream(s_in)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    for pipelined in (False, True):
+        e2e_run(3, pipelined)
     ke = max(5, min(K, 50))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world, dev)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(ke):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / ke, world, dev)
-    assert torch.equal(out2, out), "end-to-end output differs from the device-resident run"
+    e2e_serial_ms = reduce_max(e2e_run(ke, False), world, dev)
+    e2e_ms = reduce_max(e2e_run(ke, True), world, dev)
+    for z in sets:
+        assert torch.equal(z["out"], out), "end-to-end output differs from the device-resident run"
+        assert torch.equal(z["op"].to(dev), out), "copied-out result differs from the device-resident run"
 
     peak, peak_kind = measured_peak()
     cb = bytes_combine(w, kept)
@@ -426,7 +466,11 @@ def run_ours(args, rank: int, world: int, local: int):
                          "algorithmic_bytes": cb},
             "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": x.numel() * 2 + lg.numel() * 4, "d2h_bytes_per_step": out.numel() * 2,
-                    "ms_per_step": e2e_ms, "what": "H2D x+logits, route, dispatch, expert, combine, D2H out"},
+                    "ms_per_step": e2e_ms,
+                    "what": "every step: H2D x+logits from pinned host, route, dispatch, expert, combine, D2H out "
+                            "to pinned host; two buffer sets, copies of neighbouring steps overlap the compute",
+                    "serial_ms_per_step": e2e_serial_ms,
+                    "serial_value": world * w.T / (e2e_serial_ms * 1e-3)},
             "gpu_launches": 2 * KERNELS_PER_STEP * K,
             "clocks": sampler.summary(t0, t1),
             "calls": per_call,
