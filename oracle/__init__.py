@@ -25,7 +25,9 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        path = _build()
+        # MOE_ORACLE_LIB: a separately compiled copy of the oracle (the mutation
+        # tests plant one mistake in a copy and check that the pins catch it)
+        path = os.environ.get("MOE_ORACLE_LIB") or _build()
         L = C.CDLL(path)
         P = C.c_void_p
         i32, i64 = C.c_int32, C.c_int64

@@ -1,0 +1,83 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case copies oracle/moe_oracle.c, plants one mistake of the kind a
+careful reader could still make (a reversed tie rule, an off-by-one capacity
+test, an inclusive scan, rounding that truncates, a dropped term...),
+compiles the copy, and runs the oracle's pin tests against it in a fresh
+process. Every mutant must make at least one pin fail. All on the CPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    # route: equal logits go to the higher index
+    "tie_to_higher_index": ("return (a->e < b->e) ? -1 : (a->e > b->e) ? 1 : 0;",
+                            "return (a->e > b->e) ? -1 : (a->e < b->e) ? 1 : 0;"),
+    # route: the renormalisation set includes one expert too many
+    "renormalise_over_k_plus_1": ("            sum += ex[j];\n",
+                                  "            sum += ex[j] + (j == 0 && k < E ? exp((double)row[k].l - top) : 0.0);\n"),
+    # count: a pair at position C is kept
+    "capacity_off_by_one": ("slot[(int64_t)t * k + j] = (pos < C) ? pos : -1;",
+                            "slot[(int64_t)t * k + j] = (pos <= C) ? pos : -1;"),
+    # count: slots assigned choice-major instead of token-major
+    "slots_choice_major": ("    for (int32_t t = 0; t < T; ++t) {\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = topk_idx",
+                           "    for (int32_t j = 0; j < k; ++j) {\n        for (int32_t t = 0; t < T; ++t) {\n            int32_t e = topk_idx"),
+    # count: inclusive instead of exclusive scan
+    "offsets_inclusive": ("        offsets[e] = run;\n        run += cursor[e];\n",
+                          "        run += cursor[e];\n        offsets[e] = run;\n"),
+    # count: rank counts not clipped at the capacity
+    "rank_counts_unclipped": ("rank_counts[e / per_rank] += (cursor[e] < C) ? cursor[e] : C;",
+                              "rank_counts[e / per_rank] += cursor[e];"),
+    # dispatch: recv_src records the slot, not the token
+    "recv_src_is_slot": ("            memcpy(recv_x + row * H, x + (int64_t)t * H, sizeof(uint16_t) * (size_t)H);\n            recv_src[row] = t;",
+                         "            memcpy(recv_x + row * H, x + (int64_t)t * H, sizeof(uint16_t) * (size_t)H);\n            recv_src[row] = s;"),
+    # fp8 dispatch: max instead of max |x|
+    "amax_without_abs": ("float a = fabsf(bf16_decode(xr[b * 128 + i]));", "float a = bf16_decode(xr[b * 128 + i]);"),
+    # fp8 dispatch: wrong scale constant
+    "scale_447": ("amax / 448.0f", "amax / 447.0f"),
+    # e4m3: ties away from zero instead of to even
+    "e4m3_ties_up": ("c = (lo & 1u) ? hi : lo;", "c = hi;"),
+    # e4m3: subnormal exponent off by one
+    "e4m3_subnormal_exponent": ("ldexp((double)m / 8.0, 1 - 7)", "ldexp((double)m / 8.0, -7)"),
+    # bf16: truncation instead of rounding
+    "bf16_truncates": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))", "if (0)"),
+    # bf16: ties away from zero
+    "bf16_ties_up": ("(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
+    # expert: every row scaled by expert 0's scale
+    "expert_scale_index": ("v = bf16_decode(((const uint16_t *)recv)[row * H + h]) * s[e];",
+                           "v = bf16_decode(((const uint16_t *)recv)[row * H + h]) * s[0];"),
+    # combine: dropped pairs read row 0 instead of being skipped
+    "combine_keeps_dropped": ("                if (s < 0)\n                    continue;\n                int64_t row = (int64_t)topk_idx",
+                              "                if (s < 0)\n                    s = 0;\n                int64_t row = (int64_t)topk_idx"),
+    # combine: only the first choice summed
+    "combine_first_choice_only": ("            for (int32_t j = 0; j < k; ++j) {\n                int32_t s = slot",
+                                  "            for (int32_t j = 0; j < 1; ++j) {\n                int32_t s = slot"),
+    # layer stand-in: the scale factor ignored
+    "scale_rows_ignores_a": ("out[i] = bf16_encode_rne(bf16_decode(in[i]) * a);", "out[i] = bf16_encode_rne(bf16_decode(in[i]));"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    src = open(SRC).read()
+    before, after = MUTANTS[name]
+    assert src.count(before) >= 1, f"mutation site of {name} not found: the oracle changed"
+    mutated = src.replace(before, after, 1)
+    c_path = tmp_path / "moe_oracle_mutant.c"
+    so_path = tmp_path / "liboracle_mutant.so"
+    c_path.write_text(mutated)
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+                    "-o", str(so_path), str(c_path), "-lm"], check=True, capture_output=True)
+    env = dict(os.environ, MOE_ORACLE_LIB=str(so_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_codecs.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_path.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"no pin caught mutant {name}:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout
