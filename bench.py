@@ -375,6 +375,37 @@ def run_ours(args, rank: int, world: int, local: int):
         evp[i][1].record(stream)
     torch.cuda.synchronize()
     pipe_ms = reduce_max(statistics.fmean(a.elapsed_time(z) for a, z in evp), world, dev)
+    out_ref = out.clone()
+
+    # route + dispatch through the one fused call (two launches for a decode
+    # batch instead of three), cold per call and inside the pipelined step
+    def fused():
+        M.moe_route_dispatch(p, lg, x, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["slot"],
+                             b["rank_counts"], b["dropped"], b["recv"], b.get("recv_scale"), b["recv_src"],
+                             b["workspace"], stream)
+    for _ in range(3):
+        flush()
+        fused()
+    evf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    evfp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush()
+        evf[i][0].record(stream)
+        fused()
+        evf[i][1].record(stream)
+    for i in range(K):
+        flush()
+        evfp[i][0].record(stream)
+        fused()
+        calls[2][1]()
+        calls[3][1]()
+        evfp[i][1].record(stream)
+    torch.cuda.synchronize()
+    fused_ms = reduce_max(statistics.fmean(a.elapsed_time(z) for a, z in evf), world, dev)
+    fused_pipe_ms = reduce_max(statistics.fmean(a.elapsed_time(z) for a, z in evfp), world, dev)
+    assert torch.equal(out, out_ref), "fused route+dispatch changed the step's output"
     step_ms = sum(ms.values())
     dc_ms = reduce_max(ms["dispatch"] + ms["combine"], world, dev)
     step_ms_max = reduce_max(step_ms, world, dev)
@@ -478,6 +509,11 @@ def run_ours(args, rank: int, world: int, local: int):
             "pipelined": {"ms_per_step": pipe_ms, "tokens_per_s": world * w.T / (pipe_ms * 1e-3),
                           "what": "route, dispatch, expert, combine back to back (programmatic dependent "
                                   "launch), L2 flushed before each step"},
+            "fused_route_dispatch": {
+                "us": 1e3 * fused_ms, "separate_us": 1e3 * (ms["route"] + ms["dispatch"]),
+                "pipelined_ms_per_step": fused_pipe_ms, "pipelined_tokens_per_s": world * w.T / (fused_pipe_ms * 1e-3),
+                "what": "moe_route_dispatch (top-k kernel, then one kernel that forms slots and dispatches), "
+                        "L2 flushed before each call; pipelined: fused call, expert, combine"},
         }
     return line, dev
 

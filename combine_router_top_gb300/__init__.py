@@ -76,6 +76,8 @@ def lib() -> C.CDLL:
             "moe_route": ([pp, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
             "moe_route_noalloc": ([pp, P, P, P, P, P, P, P, P, P], i),
             "moe_dispatch": ([pp, P, P, P, P, P, P, P], i),
+            "moe_route_dispatch_workspace_bytes": ([pp], C.c_size_t),
+            "moe_route_dispatch": ([pp, P, P, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
             "moe_expert_synthetic": ([pp, P, P, P, P, P, P], i),
             "moe_combine": ([pp, P, P, P, P, P, P], i),
             "dbo_create": ([C.POINTER(P)], i),
@@ -95,7 +97,7 @@ def lib() -> C.CDLL:
 
 
 EXPORTS = ("moe_status_string", "moe_validate", "moe_device_status", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
-           "moe_dispatch",
+           "moe_dispatch", "moe_route_dispatch_workspace_bytes", "moe_route_dispatch",
            "moe_expert_synthetic", "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
            "moe_layer_stand_in", "dbo_layers", "dbo_layers_capture", "dbo_graph_launch")
 
@@ -164,6 +166,20 @@ def moe_dispatch(p, x, topk_idx, slot, recv, recv_scale, recv_src, stream=None):
     rc = lib().moe_dispatch(C.byref(p), _ptr(x), _ptr(topk_idx), _ptr(slot), _ptr(recv), _ptr(recv_scale),
                             _ptr(recv_src), _stream(stream))
     _check("moe_dispatch", rc)
+
+
+def moe_route_dispatch_workspace_bytes(p: moe_problem) -> int:
+    return lib().moe_route_dispatch_workspace_bytes(C.byref(p))
+
+
+def moe_route_dispatch(p, logits, x, topk_idx, topk_w, counts, offsets, slot, rank_counts, dropped, recv,
+                       recv_scale, recv_src, workspace, stream=None):
+    """moe_route then moe_dispatch in one call (fused into two launches for fp8 decode batches)."""
+    rc = lib().moe_route_dispatch(C.byref(p), _ptr(logits), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+                                  _ptr(offsets), _ptr(slot), _ptr(rank_counts), _ptr(dropped), _ptr(recv),
+                                  _ptr(recv_scale), _ptr(recv_src), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("moe_route_dispatch", rc)
 
 
 def moe_expert_synthetic(p, recv, recv_scale, counts, s, y, stream=None):
@@ -236,7 +252,7 @@ def alloc_buffers(p: moe_problem, device="cuda") -> dict:
     fp8 = p.dispatch_dtype == MOE_DTYPE_FP8_E4M3_B128
     i32 = dict(dtype=torch.int32, device=device)
     f32 = dict(dtype=torch.float32, device=device)
-    ws = moe_route_workspace_bytes(p)
+    ws = max(moe_route_workspace_bytes(p), moe_route_dispatch_workspace_bytes(p))
     if ws == 0:
         raise MoeError("moe_route_workspace_bytes", MOE_ERR_INVALID_ARG)
     b = {
@@ -253,11 +269,18 @@ def alloc_buffers(p: moe_problem, device="cuda") -> dict:
     return b
 
 
-def run_path(p: moe_problem, x, logits, s, bufs: dict, out, stream=None):
-    """route -> dispatch -> synthetic expert -> combine for one batch, on one stream."""
-    moe_route(p, logits, bufs["topk_idx"], bufs["topk_w"], bufs["counts"], bufs["offsets"], bufs["slot"],
-              bufs["rank_counts"], bufs["dropped"], bufs["workspace"], stream)
-    moe_dispatch(p, x, bufs["topk_idx"], bufs["slot"], bufs["recv"], bufs.get("recv_scale"), bufs["recv_src"], stream)
+def run_path(p: moe_problem, x, logits, s, bufs: dict, out, stream=None, fused=False):
+    """route -> dispatch -> synthetic expert -> combine for one batch, on one stream
+    (fused: route and dispatch through moe_route_dispatch)."""
+    if fused:
+        moe_route_dispatch(p, logits, x, bufs["topk_idx"], bufs["topk_w"], bufs["counts"], bufs["offsets"],
+                           bufs["slot"], bufs["rank_counts"], bufs["dropped"], bufs["recv"], bufs.get("recv_scale"),
+                           bufs["recv_src"], bufs["workspace"], stream)
+    else:
+        moe_route(p, logits, bufs["topk_idx"], bufs["topk_w"], bufs["counts"], bufs["offsets"], bufs["slot"],
+                  bufs["rank_counts"], bufs["dropped"], bufs["workspace"], stream)
+        moe_dispatch(p, x, bufs["topk_idx"], bufs["slot"], bufs["recv"], bufs.get("recv_scale"), bufs["recv_src"],
+                     stream)
     moe_expert_synthetic(p, bufs["recv"], bufs.get("recv_scale"), bufs["counts"], s, bufs["y"], stream)
     moe_combine(p, bufs["y"], bufs["topk_idx"], bufs["topk_w"], bufs["slot"], out, stream)
 

@@ -324,6 +324,171 @@ dispatch_bf16_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restri
     bulk_wait_all();                         // every store complete before the grid ends
 }
 
+// ---- fused route finalisation + fp8 dispatch, for decode-sized batches ------
+//
+// The top-k kernel of moe_route leaves, per pair, its rank within its tile of
+// 32 tokens and, per tile, the count per expert. Here one block per token t
+// stages t's bf16 row in shared memory (one bulk copy, issued before the wait
+// on the top-k kernel: x is an input of the call, final when this grid
+// starts), forms the slots of t's k choices while the copy is in flight
+// (slot_j = rank_j + the counts of expert e_j in the tiles before t's tile,
+// the tiles split over the block's threads), writes slot[] and recv_src,
+// quantises the row into shared memory and bulk-stores it to each kept
+// destination. Block 0 forms counts, offsets, rank_counts and dropped from
+// the tile counts.
+constexpr int kFusedMaxTiles = 32;             // decode-sized batches: at most 1024 tokens
+constexpr int kFusedThreads = 128;
+constexpr int kFusedMaxHidden = 16384;         // staged row + codes: 3 * H bytes of shared memory
+
+constexpr size_t fused_smem_bytes(int H, int E) {
+    return 3 * (size_t)H > 4 * (size_t)E ? 3 * (size_t)H : 4 * (size_t)E;
+}
+
+// tot: E ints of shared memory
+__device__ void fused_totals(const int32_t *__restrict__ tile_counts, int n_tiles, int E, int R, int C,
+                             int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                             int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped, int32_t *tot) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int sum = 0;
+#pragma unroll 8
+        for (int b = 0; b < n_tiles; ++b) sum += __ldcg(tile_counts + (size_t)b * E + e);
+        tot[e] = sum;
+        counts[e] = sum;
+    }
+    __syncthreads();
+    const int per_rank = E / R;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        int kept = 0;
+        for (int e = r * per_rank; e < (r + 1) * per_rank; ++e) kept += tot[e] < C ? tot[e] : C;
+        rank_counts[r] = kept;
+    }
+    if (threadIdx.x == 0) {
+        int run = 0, lost = 0;
+        for (int e = 0; e < E; ++e) {
+            offsets[e] = run;
+            run += tot[e];
+            lost += tot[e] > C ? tot[e] - C : 0;
+        }
+        offsets[E] = run;
+        *dropped = lost;
+    }
+}
+
+__global__ void __launch_bounds__(kFusedThreads)
+route_dispatch_fp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
+                          const int32_t *__restrict__ rank, const int32_t *__restrict__ tile_counts,
+                          int32_t *__restrict__ slot, uint8_t *__restrict__ recv_q, float *__restrict__ recv_scale,
+                          int32_t *__restrict__ recv_src, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                          int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped, int H, int E, int k,
+                          int C, int R, int n_tiles, unsigned *status) {
+    // the bf16 row (2H bytes), then its codes (H bytes); block 0: the E totals
+    extern __shared__ __align__(128) uint4 fused_smem[];
+    __shared__ float ss[kFusedMaxHidden / 128];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_part[kFusedThreads];
+    __shared__ int s_row[kMaxTopK];
+    __shared__ int s_n;
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (blockIdx.x == 0) {          // the totals block: first, so that it is no tail of the grid
+        pdl_enter();
+        fused_totals(tile_counts, n_tiles, E, R, C, counts, offsets, rank_counts, dropped,
+                     reinterpret_cast<int32_t *>(fused_smem));
+        return;
+    }
+    const int t = blockIdx.x - 1;
+    const int nb = H / 128, tasks = H / 16;
+    uint4 *xs = fused_smem;
+    uint4 *qs = fused_smem + tasks * 2;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_expect_tx(&bar, (uint32_t)H * 2);
+        bulk_g2s(xs, x + (size_t)t * H, (uint32_t)H * 2, &bar);
+    }
+    pdl_wait();                 // top-k kernel complete from here on; dependents launch at the end
+    // slot of each choice j: rank + counts of e_j in the tiles before t's tile
+    const int tile = t / kTileTokens;
+    const int parts = kFusedThreads / k;
+    const int e = __ldg(topk_idx + (size_t)t * k + tid % k);
+    const int my_rank = tid < k ? __ldg(rank + (size_t)t * k + tid) : 0;
+    int sum = 0;
+    if (tid < parts * k) {
+        for (int b = tid / k; b < tile; b += parts) sum += __ldcg(tile_counts + (size_t)b * E + e);
+    }
+    s_part[tid] = sum;
+    __syncthreads();
+    if (tid < 32) {
+        int dest = -1;
+        if (lane < k) {
+            int base = my_rank;
+            for (int part = 0; part < parts; ++part) base += s_part[part * k + lane];
+            const int sl = base < C ? base : -1;
+            slot[(size_t)t * k + lane] = sl;
+            if (sl >= 0) dest = e * C + sl;
+        }
+        const unsigned kept = __ballot_sync(kFull, dest >= 0);
+        if (dest >= 0) {
+            s_row[__popc(kept & ((1u << lane) - 1u))] = dest;
+            recv_src[dest] = t;
+        }
+        if (lane == 0) s_n = __popc(kept);
+    }
+    const bool ok = mbar_wait_bounded(&bar, 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            atomicOr(status, kStatusWaitGaveUp);
+            mbar_wait_bounded(&bar, 0);
+        }
+        return;
+    }
+    // 16 elements per task; the 8 tasks of a 128-element block sit in 8
+    // neighbouring lanes of one pass (the stride is a multiple of 8 and
+    // tasks % 8 == 0), so a pass is active or idle for a whole block
+    for (int pass = 0; pass < tasks; pass += kFusedThreads) {
+        const int task = pass + tid;
+        const bool on = task < tasks;
+        uint32_t wv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (on) {
+            const uint4 a = xs[2 * task], c = xs[2 * task + 1];
+            wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+            wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
+        }
+        uint32_t m = 0;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) m = bf16x2_absmax(m, wv[h]);
+        float amax = fmaxf(bf16_lo(m), bf16_hi(m));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+        if (on) {
+            const float sc = e4m3_block_scale(amax);
+            uint32_t q[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc));
+                const uint32_t hi =
+                    pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc));
+                q[h] = lo | (hi << 16);
+            }
+            qs[task] = make_uint4(q[0], q[1], q[2], q[3]);
+            if ((task & 7) == 0) ss[task >> 3] = sc;
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    const int nd = s_n;
+    if (tid == 0) {
+        for (int j = 0; j < nd; ++j) bulk_s2g(recv_q + (size_t)s_row[j] * H, qs, (uint32_t)H);
+        bulk_commit();
+    }
+    for (int i = tid; i < nd * nb; i += kFusedThreads) {
+        const int j = i / nb, blk = i - j * nb;
+        recv_scale[(size_t)s_row[j] * nb + blk] = ss[blk];
+    }
+    pdl_launch_dependents();
+    if (tid == 0) bulk_wait_all();
+}
+
 template <int U>
 int launch_fp8(const Dims &d, cudaStream_t st, const void *x, const int32_t *idx, const int32_t *slot, void *recv,
                float *scale, int32_t *src) {
@@ -408,4 +573,69 @@ extern "C" int moe_dispatch(const moe_problem *p, const void *x, const int32_t *
         case 1: return launch_bf16<1>(d, st, x, topk_idx, slot, recv, recv_src);
         default: return launch_bf16<4>(d, st, x, topk_idx, slot, recv, recv_src);
     }
+}
+
+extern "C" size_t moe_route_dispatch_workspace_bytes(const moe_problem *p) {
+    moe::Dims d;
+    if (moe::check_problem(p, &d) != MOE_OK) return 0;
+    const size_t tiles = ((size_t)d.T + moe::kTileTokens - 1) / moe::kTileTokens;
+    const size_t fused = (tiles * (size_t)d.E + (size_t)d.T * d.k) * sizeof(int32_t);
+    const size_t route = moe_route_workspace_bytes(p);
+    const size_t bytes = fused > route ? fused : route;
+    return (bytes + 255) & ~(size_t)255;
+}
+
+extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, const void *x, int32_t *topk_idx,
+                                  float *topk_w, int32_t *counts, int32_t *offsets, int32_t *slot,
+                                  int32_t *rank_counts, int32_t *dropped, void *recv, float *recv_scale,
+                                  int32_t *recv_src, void *workspace, size_t workspace_bytes, void *stream) {
+    using namespace moe;
+    Dims d;
+    int rc = check_problem(p, &d);
+    if (rc != MOE_OK) return rc;
+    if (workspace_bytes < moe_route_dispatch_workspace_bytes(p)) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = d.dtype == MOE_DTYPE_FP8_E4M3_B128;
+    const int n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
+    const bool fused = fp8 && d.H <= kFusedMaxHidden && n_tiles <= kFusedMaxTiles && d.max_blocks == 0;
+    if (!fused) {
+        rc = moe_route(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_counts, dropped, workspace,
+                       workspace_bytes, stream);
+        if (rc != MOE_OK) return rc;
+        return moe_dispatch(p, x, topk_idx, slot, recv, recv_scale, recv_src, stream);
+    }
+    // the same argument checks as moe_route and moe_dispatch
+    if (!counts || !offsets || !rank_counts || !dropped || !workspace || !recv_scale) return MOE_ERR_INVALID_ARG;
+    if (d.T > 0 && (!logits || !x || !topk_idx || !topk_w || !slot || !recv || !recv_src)) return MOE_ERR_INVALID_ARG;
+    const size_t logit_align = (d.E % 4 == 0) ? 16 : 4;
+    if (!aligned(workspace, 16) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(rank_counts, 4) ||
+        !aligned(dropped, 4) || !aligned(recv_scale, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (d.T > 0 && (!aligned(logits, logit_align) || !aligned(x, 16) || !aligned(recv, 16) ||
+                    !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(slot, 4) || !aligned(recv_src, 4)))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = as_stream(stream);
+    unsigned *status = device_status_word();
+    if (status == nullptr) return MOE_ERR_CUDA;
+    int32_t *tile_counts = static_cast<int32_t *>(workspace);
+    int32_t *rank = tile_counts + (size_t)n_tiles * d.E;
+    if (n_tiles > 0) {
+        rc = launch_route_topk(d, st, logits, topk_idx, topk_w, rank, tile_counts);
+        if (rc != MOE_OK) return rc;
+    }
+    static bool smem_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (!smem_set[dev]) {
+        if (cudaFuncSetAttribute(route_dispatch_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 fused_smem_bytes(kFusedMaxHidden, kMaxExperts)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        smem_set[dev] = true;
+    }
+    if (launch_pdl_smem(route_dispatch_fp8_kernel, d.T + 1, kFusedThreads, fused_smem_bytes(d.H, d.E), st,
+                        static_cast<const uint16_t *>(x), static_cast<const int32_t *>(topk_idx),
+                        static_cast<const int32_t *>(rank), static_cast<const int32_t *>(tile_counts), slot,
+                        static_cast<uint8_t *>(recv), recv_scale, recv_src, counts, offsets, rank_counts, dropped, d.H,
+                        d.E, d.k, d.C, d.R, n_tiles, status) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }

@@ -40,6 +40,9 @@ unsigned *device_status_word();
 constexpr unsigned kStatusWaitGaveUp = 1u;     // a bounded wait on a copy gave up
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 int sm_count();                         // SMs of the current device (cached)
+// The route's top-k / tile kernel alone (moe_route.cu), for n_tiles > 0.
+int launch_route_topk(const Dims &d, cudaStream_t st, const float *logits, int32_t *topk_idx, float *topk_w,
+                      int32_t *rank, int32_t *tile_counts);
 // moe_layer_stand_in with a cap on its grid (moe_layers.cu).
 int layer_stand_in(const void *in, void *out, int64_t n_elements, float a, int32_t busy_fmas, int max_blocks,
                    cudaStream_t st);

@@ -188,6 +188,23 @@ cudaError_t launch_topk(int n_tiles, cudaStream_t st, const float *logits, const
 }
 
 }  // namespace
+
+// The top-k / tile kernel alone (n_tiles > 0): top-k indices and weights, each
+// pair's rank within its tile into `rank`, per-tile counts into `tile_counts`.
+int launch_route_topk(const Dims &d, cudaStream_t st, const float *logits, int32_t *topk_idx, float *topk_w,
+                      int32_t *rank, int32_t *tile_counts) {
+    const int n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
+    const int per_lane = (d.E + 31) / 32;
+    cudaError_t e;
+    if (per_lane <= 1) e = launch_topk<1>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
+    else if (per_lane <= 2) e = launch_topk<2>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
+    else if (per_lane <= 4) e = launch_topk<4>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
+    else if (per_lane <= 8) e = launch_topk<8>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
+    else if (per_lane <= 16) e = launch_topk<16>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
+    else e = launch_topk<32>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace moe
 
 extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *topk_idx, float *topk_w,

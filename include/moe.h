@@ -174,6 +174,24 @@ int moe_dispatch(const moe_problem *p, const void *x,
                  const int32_t *topk_idx, const int32_t *slot,
                  void *recv, float *recv_scale, int32_t *recv_src, void *stream);
 
+/* moe_route followed by moe_dispatch in one call, with the same outputs bit
+ * for bit, for decode: [PMC §Dispatch] counts tokens per destination inside
+ * the dispatch kernel. For an fp8 dispatch with H <= 16384, at most 1024
+ * tokens and max_blocks == 0, it runs in two launches instead of three: the
+ * route's top-k kernel, then one kernel with a block per token that forms the
+ * token's slots from the per-tile counts and dispatches its row (launched as
+ * a programmatic dependent of the first). Otherwise it calls moe_route and
+ * moe_dispatch. workspace: device scratch of at least
+ * moe_route_dispatch_workspace_bytes(p) bytes, 16-byte aligned, contents
+ * needing no initialisation, not shared with a concurrent call. */
+size_t moe_route_dispatch_workspace_bytes(const moe_problem *p);
+int moe_route_dispatch(const moe_problem *p, const float *logits, const void *x,
+                       int32_t *topk_idx, float *topk_w,
+                       int32_t *counts, int32_t *offsets, int32_t *slot,
+                       int32_t *rank_counts, int32_t *dropped,
+                       void *recv, float *recv_scale, int32_t *recv_src,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
 /* Stand-in for the grouped expert GEMM that [PMC §Dispatch] feeds: on rows
  * r < min(counts[e], C) of every expert,
  *   bf16 recv:  y[e][r] = bf16(x * s[e]);

@@ -21,10 +21,11 @@ def to_host(t, dtype=None):
     return a
 
 
-def run_stages(x, logits, s, k, R, Cap, fp8, max_blocks=0, oracle_inputs=None):
+def run_stages(x, logits, s, k, R, Cap, fp8, max_blocks=0, oracle_inputs=None, fused=False):
     """The whole path on the GPU, stage by stage. With oracle_inputs (a result
     of oracle.run_path), also runs the expert and combine kernels on the
-    oracle's own upstream results, so that each stage can be compared alone."""
+    oracle's own upstream results, so that each stage can be compared alone.
+    fused: route and dispatch through the one call moe_route_dispatch."""
     T, E = logits.shape
     H = x.shape[1]
     p = M.problem(T, H, E, k, R, Cap, M.MOE_DTYPE_FP8_E4M3_B128 if fp8 else M.MOE_DTYPE_BF16, max_blocks)
@@ -32,9 +33,12 @@ def run_stages(x, logits, s, k, R, Cap, fp8, max_blocks=0, oracle_inputs=None):
     b["recv"].zero_()
     b["y"].zero_()
     b["recv_src"].fill_(-1)
+    if fp8:
+        b["recv_scale"].zero_()
+    b["workspace"].fill_(0x55)             # the workspace needs no initialisation
     xd, ld, sd = to_dev(x), to_dev(logits), to_dev(s)
     out = torch.empty((T, H), dtype=torch.int16, device=DEV)
-    M.run_path(p, xd, ld, sd, b, out)
+    M.run_path(p, xd, ld, sd, b, out, fused=fused)
     torch.cuda.synchronize()
     r = {
         "topk_idx": to_host(b["topk_idx"]), "topk_w": to_host(b["topk_w"]), "counts": to_host(b["counts"]),

@@ -88,6 +88,20 @@ def test_route_workspace_bytes(moe):
     assert moe.moe_route_workspace_bytes(mk(moe, T=33, E=8, R=2)) % 256 == 0
 
 
+def test_route_dispatch_workspace_bytes(moe):
+    p = mk(moe)        # 32 tiles x 256 experts of tile counts + 1024 x 8 ranks, int32
+    assert moe.moe_route_dispatch_workspace_bytes(p) == (32 * 256 + 1024 * 8) * 4
+    assert moe.moe_route_dispatch_workspace_bytes(p) >= moe.moe_route_workspace_bytes(p)
+    assert moe.moe_route_dispatch_workspace_bytes(mk(moe, T=0)) == 256
+    assert moe.moe_route_dispatch_workspace_bytes(mk(moe, k=0)) == 0
+    L = moe.lib()
+    fake = C.c_void_p(1 << 40)
+    args = [fake] * 12
+    assert L.moe_route_dispatch(C.byref(p), *args, fake, 16, None) == moe.MOE_ERR_INVALID_ARG
+    odd = C.c_void_p((1 << 40) + 4)
+    assert L.moe_route_dispatch(C.byref(p), odd, *args[1:], fake, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_calls_reject_bad_arguments_before_any_launch(moe):
     L = moe.lib()
     p = mk(moe)

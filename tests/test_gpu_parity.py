@@ -91,6 +91,58 @@ def test_edge_case_parity(case):
         assert o["dropped"] > 0
 
 
+FUSED = {
+    # fused kernel: fp8, H <= 16384, at most 32 tiles of 32 tokens
+    "dsv3_fp8": W.WORKLOADS["dsv3_fp8"],
+    "T1": W.WORKLOADS["dsv3_fp8"].with_(T=1),
+    "T33": W.WORKLOADS["dsv3_fp8"].with_(T=33),
+    "T1000": W.WORKLOADS["dsv3_fp8"].with_(T=1000, C=64),
+    "overflow": W.WORKLOADS["dsv3_fp8"].with_(T=500, C=3),
+    "k16_E1024": W.Workload("k16", T=97, H=1024, E=1024, k=16, R=8, C=8, dtype=1, seed=31),
+    "k3_E6": W.Workload("k3", T=45, H=2048, E=6, k=3, R=3, C=20, dtype=1, seed=32),
+    "H128_E1024": W.Workload("h128", T=70, H=128, E=1024, k=8, R=8, C=4, dtype=1, seed=34),
+    "H16384": W.Workload("h16384", T=40, H=16384, E=32, k=4, R=4, C=16, dtype=1, seed=35),
+    "H1152": W.Workload("h1152", T=64, H=1152, E=16, k=4, R=4, C=64, dtype=1, seed=33),
+    # separate calls behind the same entry point
+    "fallback_T1025": W.WORKLOADS["dsv3_fp8"].with_(T=1025, C=256),
+    "fallback_H16512": W.Workload("h16512", T=20, H=16512, E=16, k=2, R=4, C=16, dtype=1, seed=36),
+    "fallback_bf16": W.WORKLOADS["v2lite"],
+}
+
+
+@pytest.mark.parametrize("case", sorted(FUSED))
+def test_fused_route_dispatch_equals_separate_calls_and_the_oracle(case):
+    """moe_route_dispatch writes exactly what moe_route then moe_dispatch
+    write, and the whole path built on it matches the oracle."""
+    from gpu_path import compare, run_stages
+    w = FUSED[case]
+    fp8 = w.dtype == W.DTYPE_FP8_E4M3_B128
+    x, lg, s = W.make_x(w), W.make_logits(w), W.expert_scale(w)
+    a = run_stages(x, lg, s, w.k, w.R, w.C, fp8)
+    b = run_stages(x, lg, s, w.k, w.R, w.C, fp8, fused=True)
+    for key in a:
+        assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
+    o = O.run_path(x, lg, s, w.k, w.R, w.C, fp8)
+    compare(b, o, w.C, fp8)
+    if case == "overflow":
+        assert o["dropped"] > 0
+
+
+def test_fused_route_dispatch_empty_batch():
+    import torch
+    import combine_router_top_gb300 as M
+    p = M.problem(0, 7168, 256, 8, 8, 16, M.MOE_DTYPE_FP8_E4M3_B128)
+    b = M.alloc_buffers(p, "cuda:0")
+    for key in ["counts", "offsets", "rank_counts", "dropped"]:
+        b[key].fill_(-7)
+    e = torch.empty(0, device="cuda:0")
+    M.moe_route_dispatch(p, e, e, e, e, b["counts"], b["offsets"], e, b["rank_counts"], b["dropped"], e,
+                         b["recv_scale"], e, b["workspace"])
+    torch.cuda.synchronize()
+    for key in ["counts", "offsets", "rank_counts", "dropped"]:
+        assert int(b[key].abs().sum()) == 0, key
+
+
 def test_ties_and_signed_zeros():
     from gpu_path import compare
     w = W.Workload("ties", T=256, H=256, E=64, k=6, R=4, C=256, seed=21)
