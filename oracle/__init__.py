@@ -43,6 +43,8 @@ def lib():
             "oracle_expert_synthetic": [i32, i32, i32, i32, P, P, P, P, P],
             "oracle_combine": [i32, i32, i32, i32, i32, P, P, P, P, P],
             "oracle_scale_rows": [i64, P, C.c_float, P],
+            "oracle_gemm_fp8_row": [i32, i32, P, P, P, P, P],
+            "oracle_expert_gemm_fp8": [i32, i32, i32, i32, P, P, P, P, P, P],
         }.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -157,6 +159,36 @@ def expert_synthetic(recv, recv_scale, counts, s):
                                          _p(np.ascontiguousarray(counts, dtype=np.int32)),
                                          _p(np.ascontiguousarray(s, dtype=np.float32)), _p(y)),
            "oracle_expert_synthetic")
+    return y
+
+
+def expert_gemm_fp8(recv_q, recv_scale, counts, w_q, w_scale):
+    """Grouped fp8 GEMM on the dispatch layout: y[e][r] = bf16(sum over 128-blocks of
+    a_scale * w_scale * (q . w[e][n])) for r < min(counts[e], C); other rows zero.
+    recv_q [E][C][K] u8, recv_scale [E][C][K/128] f32, w_q [E][N][K] u8,
+    w_scale [E][N/128][K/128] f32 -> y [E][C][N] bf16 bits."""
+    E, Cap, K = recv_q.shape
+    N = w_q.shape[1]
+    y = np.zeros((E, Cap, N), dtype=np.uint16)
+    _check(lib().oracle_expert_gemm_fp8(K, N, E, Cap, _p(np.ascontiguousarray(recv_q, dtype=np.uint8)),
+                                        _p(np.ascontiguousarray(recv_scale, dtype=np.float32)),
+                                        _p(np.ascontiguousarray(counts, dtype=np.int32)),
+                                        _p(np.ascontiguousarray(w_q, dtype=np.uint8)),
+                                        _p(np.ascontiguousarray(w_scale, dtype=np.float32)), _p(y)),
+           "oracle_expert_gemm_fp8")
+    return y
+
+
+def gemm_fp8_row(q_row, a_scale_row, w_q_e, w_scale_e):
+    """One output row of the grouped GEMM: q_row [K] u8, a_scale_row [K/128] f32,
+    w_q_e [N][K] u8, w_scale_e [N/128][K/128] f32 -> [N] bf16 bits."""
+    N, K = w_q_e.shape
+    y = np.empty(N, dtype=np.uint16)
+    _check(lib().oracle_gemm_fp8_row(K, N, _p(np.ascontiguousarray(q_row, dtype=np.uint8)),
+                                     _p(np.ascontiguousarray(a_scale_row, dtype=np.float32)),
+                                     _p(np.ascontiguousarray(w_q_e, dtype=np.uint8)),
+                                     _p(np.ascontiguousarray(w_scale_e, dtype=np.float32)), _p(y)),
+           "oracle_gemm_fp8_row")
     return y
 
 

@@ -26,6 +26,10 @@
  *     saturation to +-448.
  *   - Combine accumulates in fp32 with one fused multiply-add per selected
  *     expert, in selection order, from 0, then rounds to bf16 (nearest-even).
+ *   - The grouped GEMM that stands in for the experts maps each dispatched
+ *     fp8 row through one random e4m3 weight matrix per expert (128 x 128
+ *     weight blocks with an fp32 scale each), exactly, then rounds once to
+ *     bf16 (nearest-even).
  *
  * Layouts (row-major):
  *   logits[T][E] f32; topk_idx[T][k] i32; topk_w[T][k] f32; slot[T][k] i32;
@@ -370,6 +374,89 @@ int oracle_expert_synthetic(int32_t H, int32_t E, int32_t C, int32_t fp8,
                 }
                 y[row * H + h] = bf16_encode_rne(v);
             }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Grouped expert GEMM on the fp8 dispatch layout (stands in for the experts  */
+/* that consume the dispatched, block-scaled tokens of [PMC §Dispatch];      */
+/* random weights, one linear map of N outputs per expert, no activation):   */
+/*   y[e][r][n] = bf16( sum_b  a_scale[e][r][b] * w_scale[e][n/128][b]        */
+/*                      * sum_{i in block b} q[e][r][i] * w[e][n][i] )        */
+/* q: the dispatched e4m3 codes, a_scale: their scale per 128 inputs;        */
+/* w[e][N][K]: e4m3 weight codes, w_scale[e][N/128][K/128]: one scale per    */
+/* 128 x 128 weight block. Each inner block sum is exact in double (an e4m3  */
+/* product has at most 8 significant bits, between 2^-18 and 2^18, and 128   */
+/* of them need fewer than 53 bits); the outer sum is taken in double and    */
+/* the result rounded once to bf16, to nearest, ties to even. The sums      */
+/* start from +0, so an exact zero comes out as +0.                          */
+/* ------------------------------------------------------------------------ */
+
+/* Nearest bf16 to a double, ties to the even code; beyond the largest      */
+/* finite bf16 (plus half an ulp) the result is infinite.                   */
+static uint16_t bf16_encode_rne_double(double v)
+{
+    if (isnan(v))
+        return 0x7FC0u;
+    const uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    int ex;
+    frexp(a, &ex);                        /* a = m * 2^ex, m in [0.5, 1)   */
+    int q = ex - 8;                       /* 8 significant bits: grid 2^q  */
+    if (q < -133)
+        q = -133;                         /* bf16 subnormal grid           */
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);   /* ties to even (default mode) */
+    if (r > 3.3895313892515355e38)        /* largest finite bf16            */
+        return sign | 0x7F80u;
+    float f = (float)r;                   /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)((u >> 16) & 0x7FFFu);
+}
+
+/* One output row: y_row[n] for n < N from one dispatched row (K inputs). */
+int oracle_gemm_fp8_row(int32_t K, int32_t N, const uint8_t *q_row, const float *a_scale_row,
+                        const uint8_t *w, const float *w_scale, uint16_t *y_row)
+{
+    if (K < 128 || N < 128 || K % 128 != 0 || N % 128 != 0)
+        return -1;
+    const int32_t kb = K / 128;
+    for (int32_t n = 0; n < N; ++n) {
+        const uint8_t *wn = w + (int64_t)n * K;
+        double acc = 0.0;
+        for (int32_t b = 0; b < kb; ++b) {
+            double block = 0.0;
+            for (int32_t i = b * 128; i < (b + 1) * 128; ++i)
+                block += (double)e4m3_decode(q_row[i]) * (double)e4m3_decode(wn[i]);
+            acc += (double)a_scale_row[b] * (double)w_scale[(int64_t)(n / 128) * kb + b] * block;
+        }
+        y_row[n] = bf16_encode_rne_double(acc);
+    }
+    return 0;
+}
+
+/* Every expert, rows r < min(counts[e], C); other rows untouched.
+ * recv_q[E][C][K], recv_scale[E][C][K/128], w[E][N][K],
+ * w_scale[E][N/128][K/128], y[E][C][N]. */
+int oracle_expert_gemm_fp8(int32_t K, int32_t N, int32_t E, int32_t C, const uint8_t *recv_q,
+                           const float *recv_scale, const int32_t *counts, const uint8_t *w,
+                           const float *w_scale, uint16_t *y)
+{
+    if (E < 1 || C < 1 || K < 128 || N < 128 || K % 128 != 0 || N % 128 != 0)
+        return -1;
+    const int32_t kb = K / 128;
+    for (int32_t e = 0; e < E; ++e) {
+        const int32_t rows = counts[e] < C ? counts[e] : C;
+        const uint8_t *we = w + (int64_t)e * N * K;
+        const float *se = w_scale + (int64_t)e * (N / 128) * kb;
+        for (int32_t r = 0; r < rows; ++r) {
+            const int64_t row = (int64_t)e * C + r;
+            if (oracle_gemm_fp8_row(K, N, recv_q + row * K, recv_scale + row * kb, we, se, y + row * N) != 0)
+                return -1;
         }
     }
     return 0;

@@ -58,6 +58,17 @@ MUTANTS = {
     # combine: only the first choice summed
     "combine_first_choice_only": ("            for (int32_t j = 0; j < k; ++j) {\n                int32_t s = slot",
                                   "            for (int32_t j = 0; j < 1; ++j) {\n                int32_t s = slot"),
+    # gemm: the weight read transposed (w[k][n] instead of w[n][k]), kept in bounds
+    "gemm_weight_transposed": ("block += (double)e4m3_decode(q_row[i]) * (double)e4m3_decode(wn[i]);",
+                               "block += (double)e4m3_decode(q_row[i]) * (double)e4m3_decode(w[(int64_t)(i % N) * K + n % K]);"),
+    # gemm: every output block takes the weight scale of output block 0
+    "gemm_weight_scale_block0": ("(double)w_scale[(int64_t)(n / 128) * kb + b]", "(double)w_scale[b]"),
+    # gemm: the activation scale of the first input block for every block
+    "gemm_activation_scale_block0": ("acc += (double)a_scale_row[b]", "acc += (double)a_scale_row[0]"),
+    # gemm: rounding through float32 first (double rounding)
+    "gemm_double_rounding": ("y_row[n] = bf16_encode_rne_double(acc);", "y_row[n] = bf16_encode_rne((float)acc);"),
+    # gemm: rows past the count computed too
+    "gemm_rows_unclipped": ("const int32_t rows = counts[e] < C ? counts[e] : C;", "const int32_t rows = C;"),
     # layer stand-in: the scale factor ignored
     "scale_rows_ignores_a": ("out[i] = bf16_encode_rne(bf16_decode(in[i]) * a);", "out[i] = bf16_encode_rne(bf16_decode(in[i]));"),
 }
@@ -77,7 +88,8 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, MOE_ORACLE_LIB=str(so_path))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_codecs.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_path.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_path.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_gemm.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"no pin caught mutant {name}:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout

@@ -24,6 +24,14 @@ Workloads (shapes of the models the pages name; no weights or datasets):
 
 x ~ bf16(float32(N(0,1))), logits ~ float32(N(0,1)) (+ float32(b_e), added in
 float32), expert scale s_e = 1 + e/E evaluated in float32.
+
+Expert weights of the grouped GEMM (random; the pages ship none) are drawn as
+storage directly, not quantised from real values: e4m3 codes with a uniform
+sign and a magnitude code uniform in 0x30..0x77 (|w| in [0.5, 240]), and one
+fp32 scale per 128 x 128 block, 2^-8 * (1 + u) with u uniform in [0, 1).
+make_weights draws them with SplitMix64 (small cases, checked by the oracle);
+make_weights_device draws the same distribution with PyTorch's seeded device
+generator (full-size runs, where a host draw of gigabytes would take minutes).
 """
 from __future__ import annotations
 
@@ -39,6 +47,9 @@ _MIX2 = 0x94D049BB133111EB
 
 STREAM_X = 1
 STREAM_LOGITS = 2
+STREAM_W = 3
+STREAM_W_SCALE = 4
+W_MAG_LO, W_MAG_N = 0x30, 72          # magnitude codes 0x30..0x77
 
 DTYPE_BF16 = 0
 DTYPE_FP8_E4M3_B128 = 1
@@ -146,3 +157,37 @@ def make_inputs(w: Workload) -> dict:
     """All host inputs of one workload: x (uint16 bf16 bits), logits, s."""
     return {"x": make_x(w), "logits": make_logits(w), "s": expert_scale(w)}
 
+
+
+def make_weights(w: Workload, e0: int = 0, ne: int | None = None, N: int | None = None):
+    """Experts e0..e0+ne-1 of the grouped GEMM's weights: e4m3 codes
+    w_q[ne][N][H] (uint8) and fp32 block scales w_scale[ne][N/128][H/128].
+    N defaults to H (an H -> H map per expert)."""
+    ne = w.E - e0 if ne is None else ne
+    N = w.H if N is None else N
+    per = N * w.H
+    z = splitmix64(_stream_key(w.seed, STREAM_W), e0 * per, ne * per)
+    r = (z >> np.uint64(32)) % np.uint64(2 * W_MAG_N)
+    mag = (r % np.uint64(W_MAG_N)).astype(np.uint8) + np.uint8(W_MAG_LO)
+    sign = (r // np.uint64(W_MAG_N)).astype(np.uint8) << np.uint8(7)
+    w_q = (mag | sign).reshape(ne, N, w.H)
+    nbs = (N // 128) * (w.H // 128)
+    u = (splitmix64(_stream_key(w.seed, STREAM_W_SCALE), e0 * nbs, ne * nbs) >> np.uint64(11)).astype(np.float64)
+    w_scale = ((1.0 + u * 2.0 ** -53) * 2.0 ** -8).astype(np.float32).reshape(ne, N // 128, w.H // 128)
+    return w_q, w_scale
+
+
+def make_weights_device(w: Workload, device, N: int | None = None):
+    """All experts' weights drawn on `device` by PyTorch's seeded generator,
+    same distribution as make_weights (not the same values)."""
+    import torch
+    N = w.H if N is None else N
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed * 65536 + STREAM_W)
+    w_q = torch.empty((w.E, N, w.H), dtype=torch.uint8, device=device)
+    for e in range(w.E):
+        r = torch.randint(0, 2 * W_MAG_N, (N, w.H), generator=g, device=device, dtype=torch.int16)
+        w_q[e] = ((r % W_MAG_N + W_MAG_LO) | ((r // W_MAG_N) << 7)).to(torch.uint8)
+    u = torch.rand((w.E, N // 128, w.H // 128), generator=g, device=device, dtype=torch.float64)
+    w_scale = ((1.0 + u) * 2.0 ** -8).to(torch.float32)
+    return w_q, w_scale
