@@ -79,6 +79,7 @@ def lib() -> C.CDLL:
             "moe_route_dispatch_workspace_bytes": ([pp], C.c_size_t),
             "moe_route_dispatch": ([pp, P, P, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
             "moe_expert_synthetic": ([pp, P, P, P, P, P, P], i),
+            "moe_expert_gemm_fp8": ([pp, P, P, P, P, P, P, P], i),
             "moe_combine": ([pp, P, P, P, P, P, P], i),
             "dbo_create": ([C.POINTER(P)], i),
             "dbo_destroy": ([P], None),
@@ -98,7 +99,7 @@ def lib() -> C.CDLL:
 
 EXPORTS = ("moe_status_string", "moe_validate", "moe_device_status", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
            "moe_dispatch", "moe_route_dispatch_workspace_bytes", "moe_route_dispatch",
-           "moe_expert_synthetic", "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
+           "moe_expert_synthetic", "moe_expert_gemm_fp8", "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
            "moe_layer_stand_in", "dbo_layers", "dbo_layers_capture", "dbo_graph_launch")
 
 
@@ -186,6 +187,13 @@ def moe_expert_synthetic(p, recv, recv_scale, counts, s, y, stream=None):
     rc = lib().moe_expert_synthetic(C.byref(p), _ptr(recv), _ptr(recv_scale), _ptr(counts), _ptr(s), _ptr(y),
                                     _stream(stream))
     _check("moe_expert_synthetic", rc)
+
+
+def moe_expert_gemm_fp8(p, recv_q, recv_scale, counts, w_q, w_scale, y, stream=None):
+    """Grouped fp8 GEMM on the dispatch layout (tensor cores): y[e][r] = bf16(row . W_e^T) on kept rows."""
+    rc = lib().moe_expert_gemm_fp8(C.byref(p), _ptr(recv_q), _ptr(recv_scale), _ptr(counts), _ptr(w_q),
+                                   _ptr(w_scale), _ptr(y), _stream(stream))
+    _check("moe_expert_gemm_fp8", rc)
 
 
 def moe_combine(p, y, topk_idx, topk_w, slot, out, stream=None):

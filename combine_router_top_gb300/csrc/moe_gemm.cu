@@ -1,0 +1,336 @@
+// moe_gemm.cu -- grouped fp8 GEMM on the dispatch layout, on the tcgen05
+// tensor cores: the experts that consume the block-scaled tokens of
+// "Efficient and portable mixture-of-experts communication" (§Dispatch), with
+// random weights standing in for trained ones.
+//
+//   y[e][r][n] = bf16( sum_b a_scale[e][r][b] * w_scale[e][n/128][b]
+//                      * sum_{i in block b} q[e][r][i] * w[e][n][i] )
+//
+// for r < min(counts[e], C), n < H, blocks b of 128 inputs. q and w are e4m3.
+//
+// One CTA computes a 128 x 128 tile (128 rows of one expert, 128 outputs):
+//   warp 0      one lane issues the TMA loads of the A (rows) and B (weights)
+//               128 x 128-byte tiles, 128-byte swizzled, into a 3-stage ring;
+//   warp 1      allocates 256 TMEM columns; one lane issues, per block b,
+//               four tcgen05.mma kind::f8f6f4 (K = 32 each) into one of two
+//               128-column fp32 accumulators, fresh for every b;
+//   warps 2..9  read the block's accumulator (tcgen05.ld), release it, and add
+//               it times a_scale[r][b] * w_scale[n/128][b] into 64 registers per
+//               thread (two warps per 32-lane TMEM quadrant, 64 columns each);
+//               after the last block they round to bf16 and store the rows.
+// The fp32 scales of both operands change with b, so the per-block partial
+// sums are scaled outside the tensor core (the hardware block-scaled MMA
+// takes power-of-two scales per 32 elements, not these).
+//
+// Every mbarrier wait is bounded. A wait that gives up raises the device
+// status word and a CTA-wide abort flag; the CTA then drains its copies and
+// MMAs in flight (again bounded), frees its TMEM and returns.
+#include "moe_internal.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int kGemmTile = 128;                  // rows, outputs and inputs per tile / block
+constexpr int kGemmStages = 3;
+constexpr int kGemmEpiWarps = 8;
+constexpr int kGemmThreads = 32 * (2 + kGemmEpiWarps);
+constexpr uint32_t kGemmTileBytes = kGemmTile * kGemmTile;     // one e4m3 tile: 16 KB
+constexpr uint32_t kGemmStageBytes = 2 * kGemmTileBytes;
+constexpr uint32_t kGemmTmemCols = 2 * kGemmTile;              // two fp32 accumulators
+constexpr size_t kGemmSmemBytes = kGemmStages * kGemmStageBytes + 1024;   // + alignment slack
+constexpr unsigned kGemmPollLimit = 1u << 20;
+
+// Shared-memory matrix descriptor of a K-major tile whose rows are 128 bytes,
+// 128-byte swizzled (as TMA writes it): 8-row swizzle atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);           // start address
+    d |= (uint64_t)(1024u >> 4) << 32;                           // stride byte offset
+    d |= (uint64_t)1 << 46;                                      // descriptor version
+    d |= (uint64_t)2 << 61;                                      // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f8f6f4, A and B e4m3, both K-major, fp32
+// accumulator, M = N = 128.
+constexpr uint32_t kIdescF8 = (1u << 4)                          // D format f32
+                              | (0u << 7) | (0u << 10)           // A, B e4m3
+                              | ((uint32_t)(kGemmTile >> 3) << 17)   // N / 8
+                              | ((uint32_t)(kGemmTile >> 4) << 24);  // M / 16
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(kIdescF8), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on the mbarrier when every MMA this thread issued so far is complete.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Bounded wait on phase `parity`; gives up early once another role aborted.
+__device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    for (unsigned i = 0; i < kGemmPollLimit; ++i) {
+        uint32_t done;
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                     : "=r"(done)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        if (done) return true;
+        if ((i & 1023u) == 1023u && *abort_flag) return false;
+    }
+    *abort_flag = 1;
+    return false;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 2)
+expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                       const float *__restrict__ a_scale, const int32_t *__restrict__ counts,
+                       const float *__restrict__ w_scale, uint16_t *__restrict__ y, int H, int C, int n_tiles,
+                       int m_tiles, unsigned *status) {
+    extern __shared__ uint8_t gemm_smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kGemmStages], empty_bar[kGemmStages];
+    __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x % m_tiles;
+    const int nt = (blockIdx.x / m_tiles) % n_tiles;
+    const int e = blockIdx.x / (m_tiles * n_tiles);
+    const int nkb = H / kGemmTile;
+    const uint32_t smem0 = (smem_u32(gemm_smem_raw) + 1023u) & ~1023u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGemmStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull_bar[b], 1);
+            mbar_init(&tempty_bar[b], kGemmEpiWarps);
+        }
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    pdl_wait();                                   // counts and the dispatched rows are final from here on
+    const int kept = min(__ldg(counts + e), C);
+    const int rows = min(kept - mt * kGemmTile, kGemmTile);
+    if (rows <= 0) {                              // no row of this expert in this tile
+        pdl_launch_dependents();
+        return;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kGemmTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    int issued = 0;                               // producer: stages loaded
+    int committed = 0;                            // MMA issuer: blocks committed
+    if (warp == 0) {
+        if (lane == 0) {
+            const int row_a = e * C + mt * kGemmTile;
+            const int row_b = e * H + nt * kGemmTile;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kGemmStages;
+                if (kb >= kGemmStages &&
+                    !gemm_wait(smem_u32(&empty_bar[s]), ((kb / kGemmStages) + 1) & 1, &s_abort))
+                    break;
+                const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kGemmTileBytes;
+                mbar_expect_tx(&full_bar[s], kGemmStageBytes);
+                tma_load_2d(sa, &map_a, smem_u32(&full_bar[s]), kb * kGemmTile, row_a);
+                tma_load_2d(sb, &map_b, smem_u32(&full_bar[s]), kb * kGemmTile, row_b);
+                issued = kb + 1;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kGemmStages, buf = kb & 1;
+                if (!gemm_wait(smem_u32(&full_bar[s]), (kb / kGemmStages) & 1, &s_abort)) break;
+                if (kb >= 2 && !gemm_wait(smem_u32(&tempty_bar[buf]), ((kb >> 1) + 1) & 1, &s_abort)) break;
+                tc_fence_after();
+                const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kGemmTileBytes;
+                const uint32_t d = tmem + buf * kGemmTile;
+#pragma unroll
+                for (int k = 0; k < kGemmTile / 32; ++k)
+                    mma_f8(d, umma_desc_sw128(sa + 32 * k), umma_desc_sw128(sb + 32 * k), k > 0 ? 1u : 0u);
+                mma_commit(smem_u32(&empty_bar[s]));
+                mma_commit(smem_u32(&tfull_bar[buf]));
+                committed = kb + 1;
+            }
+        }
+    } else {
+        const int quad = warp & 3;                        // TMEM lanes this warp may read
+        const int half = (warp - 2) >> 2;                 // which 64 of the 128 columns
+        const int r = quad * 32 + lane;                   // row within the tile
+        const bool live = r < rows;
+        const size_t grow = (size_t)e * C + (size_t)mt * kGemmTile + r;
+        const float *sa_row = a_scale + grow * nkb;
+        const float *sw_row = w_scale + ((size_t)e * n_tiles + nt) * nkb;
+        float acc[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        float f_next = live ? __ldg(sa_row) * __ldg(sw_row) : 0.0f;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int buf = kb & 1;
+            const float f = f_next;
+            if (kb + 1 < nkb) f_next = live ? __ldg(sa_row + kb + 1) * __ldg(sw_row + kb + 1) : 0.0f;
+            int got = 0;
+            if (lane == 0) got = gemm_wait(smem_u32(&tfull_bar[buf]), (kb >> 1) & 1, &s_abort) ? 1 : 0;
+            if (!__shfl_sync(kFull, got, 0)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * kGemmTile + half * 64;
+            uint32_t v[4][16];
+            tmem_ld16(taddr + 0, v[0]);
+            tmem_ld16(taddr + 16, v[1]);
+            tmem_ld16(taddr + 32, v[2]);
+            tmem_ld16(taddr + 48, v[3]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(__uint_as_float(v[c][j]), f, acc[c * 16 + j]);
+        }
+        if (ok && live) {
+            uint4 *dst = reinterpret_cast<uint4 *>(y + grow * H + (size_t)nt * kGemmTile + half * 64);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                dst[c] = make_uint4(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                                    pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+        }
+    }
+    pdl_launch_dependents();
+    tc_fence_before();
+    __syncthreads();
+    if (s_abort) {
+        // drain: the loads and MMAs this CTA started must land before its
+        // shared memory and TMEM are released
+        volatile int no_abort = 0;
+        if (warp == 0 && lane == 0) {
+            atomicOr(status, kStatusWaitGaveUp);
+            for (int kb = (issued > kGemmStages ? issued - kGemmStages : 0); kb < issued; ++kb)
+                gemm_wait(smem_u32(&full_bar[kb % kGemmStages]), (kb / kGemmStages) & 1, &no_abort);
+        }
+        if (warp == 1 && lane == 0 && committed > 0)
+            gemm_wait(smem_u32(&tfull_bar[(committed - 1) & 1]), ((committed - 1) >> 1) & 1, &no_abort);
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGemmTmemCols)
+                     : "memory");
+    }
+}
+
+// ---- host: tensor maps --------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A [rows][cols] byte matrix read in 128 x 128 tiles, 128-byte swizzled;
+// rows past the end read as zero.
+bool encode_tile_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {kGemmTile, kGemmTile};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_expert_gemm_fp8(const moe_problem *p, const void *recv_q, const float *recv_scale,
+                                   const int32_t *counts, const void *w_q, const float *w_scale, void *y,
+                                   void *stream) {
+    using namespace moe;
+    Dims d;
+    int rc = check_problem(p, &d);
+    if (rc != MOE_OK) return rc;
+    if (d.dtype != MOE_DTYPE_FP8_E4M3_B128) return MOE_ERR_UNSUPPORTED;
+    if (!recv_q || !recv_scale || !counts || !w_q || !w_scale || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned(recv_q, 16) || !aligned(w_q, 16) || !aligned(y, 16) || !aligned(recv_scale, 4) ||
+        !aligned(w_scale, 4) || !aligned(counts, 4))
+        return MOE_ERR_INVALID_ARG;
+    CUtensorMap map_a, map_b;
+    if (!encode_tile_map(&map_a, recv_q, (uint64_t)d.E * d.C, (uint64_t)d.H) ||
+        !encode_tile_map(&map_b, w_q, (uint64_t)d.E * d.H, (uint64_t)d.H))
+        return MOE_ERR_CUDA;
+    unsigned *status = device_status_word();
+    if (status == nullptr) return MOE_ERR_CUDA;
+    static bool smem_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (!smem_set[dev]) {
+        if (cudaFuncSetAttribute(expert_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kGemmSmemBytes) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        smem_set[dev] = true;
+    }
+    const int n_tiles = d.H / kGemmTile;
+    const int m_tiles = (d.C + kGemmTile - 1) / kGemmTile;
+    const long long grid = (long long)d.E * n_tiles * m_tiles;
+    if (grid > 0x7FFFFFFFLL) return MOE_ERR_UNSUPPORTED;
+    if (launch_pdl_smem(expert_gemm_fp8_kernel, (int)grid, kGemmThreads, kGemmSmemBytes, as_stream(stream), map_a,
+                        map_b, recv_scale, counts, w_scale, static_cast<uint16_t *>(y), d.H, d.C, n_tiles, m_tiles,
+                        status) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}

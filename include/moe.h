@@ -201,6 +201,26 @@ int moe_route_dispatch(const moe_problem *p, const float *logits, const void *x,
 int moe_expert_synthetic(const moe_problem *p, const void *recv, const float *recv_scale,
                          const int32_t *counts, const float *s, void *y, void *stream);
 
+/* Grouped expert GEMM on the fp8 dispatch layout, on the tensor cores: the
+ * experts that consume the block-scaled dispatched tokens of [PMC §Dispatch],
+ * one H -> H linear map per expert with random weights (no activation):
+ *   y[e][r][n] = bf16( sum_b recv_scale[e][r][b] * w_scale[e][n/128][b]
+ *                      * sum_{i in block b} recv_q[e][r][i] * w_q[e][n][i] )
+ * for r < min(counts[e], C), n < H, blocks b of 128 inputs; other rows of y
+ * are not written. Each block's sum runs on the tensor cores in fp32, is
+ * multiplied by fl(recv_scale * w_scale) and accumulated with one fp32 FMA per
+ * block in ascending b, then rounded to bf16 (nearest even).
+ * Layouts (device, row-major): recv_q u8[E][C][H] and recv_scale f32[E][C][H/128]
+ * as moe_dispatch writes them; w_q u8[E][H][H] e4m3 codes, output index major
+ * (row n holds the H inputs of output n); w_scale f32[E][H/128][H/128]; y bf16
+ * [E][C][H]; counts i32[E] as moe_route writes them. recv_q, w_q and y 16-byte
+ * aligned. Requires dispatch_dtype == MOE_DTYPE_FP8_E4M3_B128 (else
+ * MOE_ERR_UNSUPPORTED); max_blocks is ignored (one CTA per 128 x 128 output
+ * tile). Launched as a programmatic dependent of the previous kernel. */
+int moe_expert_gemm_fp8(const moe_problem *p, const void *recv_q, const float *recv_scale,
+                        const int32_t *counts, const void *w_q, const float *w_scale,
+                        void *y, void *stream);
+
 /* Step 4: combine. [PMC §Combine]: the expert outputs are read back through
  * the routing table and summed with the router weights into an externally
  * allocated tensor:

@@ -102,6 +102,21 @@ def test_route_dispatch_workspace_bytes(moe):
     assert L.moe_route_dispatch(C.byref(p), odd, *args[1:], fake, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_gemm_rejects_bad_arguments_before_any_launch(moe):
+    L = moe.lib()
+    p, pb = mk(moe), mk(moe, dtype=0)
+    fake = C.c_void_p(1 << 40)
+    odd = C.c_void_p((1 << 40) + 8)
+    args = [fake] * 6
+    assert L.moe_expert_gemm_fp8(C.byref(pb), *args, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_expert_gemm_fp8(None, *args, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_expert_gemm_fp8(C.byref(p), None, *args[1:], None) == moe.MOE_ERR_INVALID_ARG
+    for i in (0, 3, 5):                      # recv_q, w_q, y need 16-byte alignment
+        a = list(args)
+        a[i] = odd
+        assert L.moe_expert_gemm_fp8(C.byref(p), *a, None) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_calls_reject_bad_arguments_before_any_launch(moe):
     L = moe.lib()
     p = mk(moe)

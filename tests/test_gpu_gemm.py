@@ -1,0 +1,162 @@
+"""GPU parity of the grouped fp8 GEMM on the tensor cores against the oracle.
+
+The kernel is fed the oracle's own dispatch output (rows past each expert's
+count filled with random codes, NaN codes included, which must not leak into
+kept rows), and the seeded weights.
+
+Tolerance, from the arithmetic: the kernel sums each 128-input block on the
+tensor cores in fp32 (products of two e4m3 values are exact; the sum rounds),
+scales it by fl(a_scale * w_scale) and accumulates blocks with one fp32 FMA
+each, then rounds to bf16; the oracle is exact until one final bf16 rounding.
+With S = sum_b |a_scale * w_scale| * sum_i |q_i * w_i| the bound is
+    |y_gpu - y_oracle| <= 2^-12 * S + 2^-20 * S + 1 bf16 ulp of y_oracle,
+granting the block sum 12 correct bits relative to its absolute sum, the
+scale product and FMA chain 2^-20, and one ulp for the two bf16 roundings.
+A wrong element, block, scale or transposition is off by O(S).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+SENTINEL = 0xFFFF
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from combine_router_top_gb300 import build as B
+    B.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def e4m3_abs(codes):
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).abs().numpy()
+
+
+def bf16_f64(bits):
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def abs_bound_row(q_row, sa_row, w_e, sw_e):
+    """S[n] for one row: sum_b |sa_b * sw[n/128][b]| * sum_{i in b} |q_i| |w[n][i]|."""
+    N, K = w_e.shape
+    qa, wa = e4m3_abs(q_row), e4m3_abs(w_e)
+    S = np.zeros(N)
+    for b in range(K // 128):
+        blk = wa[:, b * 128:(b + 1) * 128] @ qa[b * 128:(b + 1) * 128]
+        S += blk * np.abs(sa_row[b] * np.repeat(sw_e[:, b].astype(np.float64), 128))
+    return S
+
+
+def check_row(y_gpu, y_ref, S):
+    g, r = bf16_f64(y_gpu), bf16_f64(y_ref)
+    assert np.all(np.isfinite(g)), "non-finite output"
+    a = np.abs(r)
+    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 7), 2.0 ** -133)
+    tol = (2.0 ** -12 + 2.0 ** -20) * S + ulp
+    err = np.abs(g - r)
+    assert np.all(err <= tol), f"max err/S {np.max(err / np.maximum(S, 1e-300)):.3g}"
+    return float(np.max(err / np.maximum(S, 1e-300)))
+
+
+def oracle_dispatch(w: W.Workload):
+    x, lg = W.make_x(w), W.make_logits(w)
+    idx, _ = O.route(lg, w.k)
+    c = O.count(idx, w.E, w.R, w.C)
+    rq, rs, _ = O.dispatch_fp8(x, idx, c["slot"], w.E, w.C)
+    return rq, rs, c["counts"]
+
+
+def run_gemm(w: W.Workload, rq, rs, counts, wq, ws):
+    import combine_router_top_gb300 as M
+    E, C, H = rq.shape
+    rng = np.random.default_rng(w.seed)
+    rq_dev = rq.copy()
+    rs_dev = rs.copy()
+    for e in range(E):                        # rows past the count: garbage, NaN codes included
+        kept = min(int(counts[e]), C)
+        rq_dev[e, kept:] = rng.integers(0, 256, size=(C - kept, H), dtype=np.uint8)
+        rs_dev[e, kept:] = np.nan
+    p = M.problem(w.T, H, E, w.k, w.R, C, M.MOE_DTYPE_FP8_E4M3_B128)
+    y = torch.full((E, C, H), SENTINEL, dtype=torch.int32, device=DEV).to(torch.int16)
+    M.moe_expert_gemm_fp8(p, torch.from_numpy(rq_dev).to(DEV), torch.from_numpy(rs_dev).to(DEV),
+                          torch.from_numpy(np.ascontiguousarray(counts, dtype=np.int32)).to(DEV),
+                          torch.from_numpy(wq).to(DEV), torch.from_numpy(ws).to(DEV), y)
+    torch.cuda.synchronize()
+    assert M.moe_device_status() == M.MOE_OK
+    return y.cpu().numpy().view(np.uint16)
+
+
+CASES = {
+    # one input block; partial last tile (C = 40 < 128)
+    "H128": (W.Workload("g128", T=60, H=128, E=3, k=2, R=1, C=40, dtype=1, seed=201), None),
+    # as many blocks as pipeline stages
+    "H384": (W.Workload("g384", T=100, H=384, E=4, k=2, R=2, C=64, dtype=1, seed=202), None),
+    # two row tiles per expert (C = 160), the stage ring wrapping
+    "H512_two_row_tiles": (W.Workload("g512", T=150, H=512, E=2, k=2, R=1, C=160, dtype=1, seed=203), None),
+    # many blocks
+    "H2048": (W.Workload("g2048", T=24, H=2048, E=2, k=2, R=2, C=32, dtype=1, seed=204), None),
+    # overflowing experts (counts > C) and experts forced empty
+    "overflow_and_empty": (W.Workload("gov", T=64, H=256, E=8, k=2, R=4, C=8, dtype=1, seed=205), [1, 6]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_gemm_matches_oracle(case):
+    w, empty = CASES[case]
+    rq, rs, counts = oracle_dispatch(w)
+    counts = counts.copy()
+    if empty:
+        counts[empty] = 0
+    wq, ws = W.make_weights(w)
+    y_ref = O.expert_gemm_fp8(rq, rs, counts, wq, ws)
+    y = run_gemm(w, rq, rs, counts, wq, ws)
+    worst = 0.0
+    for e in range(w.E):
+        kept = min(int(counts[e]), w.C)
+        assert np.all(y[e, kept:] == SENTINEL), f"expert {e}: rows past the count were written"
+        for r in range(kept):
+            worst = max(worst, check_row(y[e, r], y_ref[e, r], abs_bound_row(rq[e, r], rs[e, r], wq[e], ws[e])))
+    print(f"{case}: max |err| / S = {worst:.3g}")
+
+
+def test_gemm_dsv3_full_size_sampled_rows():
+    """DeepSeek-V3 decode shape (1024 tokens, H 7168, 256 experts, C 128): the
+    whole chain route -> dispatch -> GEMM on the GPU, 13 GB of device-drawn
+    weights; sampled rows against the oracle's row entry fed by the oracle's
+    own dispatch; every row past a count untouched."""
+    import combine_router_top_gb300 as M
+    w = W.WORKLOADS["dsv3_fp8"]
+    rq, rs, counts = oracle_dispatch(w)
+    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
+    b = M.alloc_buffers(p, DEV)
+    x = torch.from_numpy(W.make_x(w).view(np.int16)).to(DEV)
+    lg = torch.from_numpy(W.make_logits(w)).to(DEV)
+    M.moe_route(p, lg, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["slot"], b["rank_counts"],
+                b["dropped"], b["workspace"])
+    M.moe_dispatch(p, x, b["topk_idx"], b["slot"], b["recv"], b["recv_scale"], b["recv_src"])
+    wq, ws = W.make_weights_device(w, DEV)
+    y = torch.full((w.E, w.C, w.H), SENTINEL, dtype=torch.int32, device=DEV).to(torch.int16)
+    M.moe_expert_gemm_fp8(p, b["recv"], b["recv_scale"], b["counts"], wq, ws, y)
+    torch.cuda.synchronize()
+    assert M.moe_device_status() == M.MOE_OK
+    assert np.array_equal(b["counts"].cpu().numpy(), counts)
+    yh = y.cpu().numpy().view(np.uint16)
+    kept = np.minimum(counts, w.C)
+    for e in range(w.E):
+        assert np.all(yh[e, kept[e]:] == SENTINEL)
+    live = [e for e in range(w.E) if kept[e] > 0]
+    picks = [(live[0], 0), (live[0], kept[live[0]] - 1), (live[len(live) // 2], 1 % kept[live[len(live) // 2]]),
+             (live[-1], kept[live[-1]] - 1), (live[-1], 0), (live[len(live) // 3], kept[live[len(live) // 3]] // 2)]
+    worst = 0.0
+    for e, r in picks:
+        wq_e, ws_e = wq[e].cpu().numpy(), ws[e].cpu().numpy()
+        ref = O.gemm_fp8_row(rq[e, r], rs[e, r], wq_e, ws_e)
+        worst = max(worst, check_row(yh[e, r], ref, abs_bound_row(rq[e, r], rs[e, r], wq_e, ws_e)))
+    print(f"dsv3 sampled rows: max |err| / S = {worst:.3g}")
