@@ -23,6 +23,9 @@ by CUDA events on its stream and the flush is outside the brackets.
                names): algorithmic bytes / mean duration vs measured HBM peak.
   cpu_baseline the CPU oracle, single-threaded, on a bounded sample.
   dbo          the dual-batch-overlap step on the 8192-token prefill workload.
+  expert_gemm  the grouped fp8 GEMM on the tensor cores (random weights) at the
+               decode shape (HBM roofline) and an 8192-token prefill shape
+               (tensor roofline), and the decode step with it.
 
 --impl reference times the CPU oracle instead (the reference arm of this
 build), on a bounded sample of the same workload.
@@ -93,6 +96,34 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_PER_BF16 = 2.0            # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
+
+
+def measured_fp8_peak():
+    """Dense fp8 tensor peak in TFLOP/s: the measured bf16 GEMM peak (burst and
+    sustained) times the nominal fp8:bf16 ratio."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            j = json.load(fh)
+        return (FP8_PER_BF16 * float(j["bf16_tflops"]), FP8_PER_BF16 * float(j["bf16_tflops_sustained"]),
+                "measured bf16 x 2")
+    except Exception:
+        return FP8_PER_BF16 * FALLBACK_BF16_TFLOPS, FP8_PER_BF16 * 1700.0, "fallback bf16 x 2"
+
+
+_X_CACHE = {}
+
+
+def x_of(w: W.Workload):
+    """Host token rows of a workload, drawn once per (seed, T, H)."""
+    key = (w.seed, w.T, w.H)
+    if key not in _X_CACHE:
+        _X_CACHE[key] = W.make_x(w)
+    return _X_CACHE[key]
+
+
 def kernel_source_sha(files) -> str:
     h = hashlib.sha256()
     for f in files:
@@ -102,7 +133,8 @@ def kernel_source_sha(files) -> str:
 
 
 TRAFFIC_SOURCES = {"combine": ["moe_combine.cu", "moe_internal.cuh"],
-                   "dispatch": ["moe_dispatch.cu", "moe_internal.cuh"]}
+                   "dispatch": ["moe_dispatch.cu", "moe_internal.cuh"],
+                   "gemm": ["moe_gemm.cu", "moe_internal.cuh"]}
 
 
 def ncu_traffic(kernel: str, workload: str):
@@ -525,7 +557,7 @@ def run_dbo(args, dev) -> dict:
     w = W.WORKLOADS["dbo"]
     T0, T1 = w.T // 2, w.T - w.T // 2
     pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C)
-    x = torch.from_numpy(W.make_x(w).view(np.int16)).to(dev)
+    x = torch.from_numpy(x_of(w).view(np.int16)).to(dev)
     lg = torch.from_numpy(W.make_logits(w)).to(dev)
     s = torch.from_numpy(W.expert_scale(w)).to(dev)
     bufs = [M.alloc_buffers(M.problem(T1, w.H, w.E, w.k, w.R, w.C), dev) for _ in range(2)]
@@ -581,7 +613,7 @@ def run_dbo_layers(args, dev, layers: int = 4, busy_fmas: int = 256) -> dict:
     w = W.WORKLOADS["dbo"]
     T1 = w.T - w.T // 2
     pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C)
-    x = torch.from_numpy(W.make_x(w).view(np.int16)).to(dev)
+    x = torch.from_numpy(x_of(w).view(np.int16)).to(dev)
     lg = torch.from_numpy(np.stack([W.make_logits(w.with_(seed=w.seed + 31 * l)) for l in range(layers)])).to(dev)
     s = torch.from_numpy(W.expert_scale(w)).to(dev)
     bufs = [M.alloc_buffers(M.problem(T1, w.H, w.E, w.k, w.R, w.C), dev) for _ in range(2)]
@@ -621,6 +653,93 @@ def run_dbo_layers(args, dev, layers: int = 4, busy_fmas: int = 256) -> dict:
             "l2": "flushed before every run of the layers"}
 
 
+def run_gemm(args, dev, reps: int = 10, experts: int = 0) -> dict:
+    """The grouped fp8 GEMM on the tensor cores, fed by route + dispatch, at the
+    DeepSeek-V3 decode shape (weight-streaming, bound by HBM) and at an
+    8192-token prefill shape (bound by the tensor cores); plus the decode step
+    with the GEMM in place of the synthetic expert. Weights (13.2 GB) and
+    activations far exceed L2, so no flush is needed between calls."""
+    import torch
+    import combine_router_top_gb300 as M
+    hbm, hbm_kind = measured_peak()
+    fp8_burst, fp8_sust, fp8_kind = measured_fp8_peak()
+    st = torch.cuda.current_stream()
+    out = {}
+    wq = ws = None
+    cases = [("decode", W.WORKLOADS["dsv3_fp8"]), ("prefill", W.WORKLOADS["dbo"].with_(dtype=1))]
+    if experts:                                   # a smaller case with the same shapes per expert (profiling)
+        cases = [(n, w.with_(E=experts, R=min(w.R, experts))) for n, w in cases]
+    for name, w in cases:
+        p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
+        b = M.alloc_buffers(p, dev)
+        x = torch.from_numpy(x_of(w).view(np.int16)).to(dev)
+        lg = torch.from_numpy(W.make_logits(w)).to(dev)
+        M.moe_route(p, lg, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["slot"], b["rank_counts"],
+                    b["dropped"], b["workspace"], st)
+        M.moe_dispatch(p, x, b["topk_idx"], b["slot"], b["recv"], b["recv_scale"], b["recv_src"], st)
+        if wq is None:
+            wq, ws = W.make_weights_device(w, dev)
+        y = torch.empty((w.E, w.C, w.H), dtype=torch.int16, device=dev)
+
+        def gemm():
+            M.moe_expert_gemm_fp8(p, b["recv"], b["recv_scale"], b["counts"], wq, ws, y, st)
+        for _ in range(3):
+            gemm()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a, z in ev:
+            a.record(st)
+            gemm()
+            z.record(st)
+        torch.cuda.synchronize()
+        ms = statistics.fmean(a.elapsed_time(z) for a, z in ev)
+        counts = b["counts"].cpu().numpy()
+        kept = int(np.minimum(counts, w.C).sum())
+        active = int((counts > 0).sum())
+        nb = w.H // 128
+        algo_bytes = active * (w.H * w.H + nb * nb * 4) + kept * (w.H + nb * 4) + kept * w.H * 2 + w.E * 4
+        flops = 2.0 * kept * w.H * w.H
+        gbs, tfs = algo_bytes / (ms * 1e-3) / 1e9, flops / (ms * 1e-3) / 1e12
+        r = {"workload": f"{name}: T={w.T}, H={w.H}, E={w.E}, top_k={w.k}, C={w.C}, kept rows {kept}, "
+                         f"{active} experts with rows, fp8 e4m3 in, bf16 out",
+             "ms": ms, "algorithmic_bytes": algo_bytes, "flops": flops, "GB/s": gbs, "TFLOP/s": tfs,
+             "reps": reps}
+        if name == "decode":
+            # the 32-expert capture, scaled to this launch by the ratio of algorithmic bytes
+            # (weights dominate both; every kept row of the 32-expert decode case is full: 32 x 128)
+            t32 = ncu_traffic("gemm", "dsv3_fp8_E32")
+            algo32 = 32 * (w.H * w.H + nb * nb * 4) + 32 * 128 * (w.H + nb * 4) + 32 * 128 * w.H * 2 + 32 * 4
+            traffic = None if t32 is None else int(t32 * algo_bytes / algo32)
+            r["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                             "peak_source": f"{hbm_kind} hbm_gbs", "traffic": traffic}
+            s = torch.from_numpy(W.expert_scale(w)).to(dev)
+            outp = torch.empty((w.T, w.H), dtype=torch.int16, device=dev)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for i in range(reps + 3):
+                if i >= 3:
+                    evs[i - 3][0].record(st)
+                M.moe_route(p, lg, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["slot"],
+                            b["rank_counts"], b["dropped"], b["workspace"], st)
+                M.moe_dispatch(p, x, b["topk_idx"], b["slot"], b["recv"], b["recv_scale"], b["recv_src"], st)
+                gemm()
+                M.moe_combine(p, y, b["topk_idx"], b["topk_w"], b["slot"], outp, st)
+                if i >= 3:
+                    evs[i - 3][1].record(st)
+            torch.cuda.synchronize()
+            step_ms = statistics.fmean(a.elapsed_time(z) for a, z in evs)
+            r["step_with_gemm"] = {"ms_per_step": step_ms, "tokens_per_s": w.T / (step_ms * 1e-3),
+                                   "what": "route, dispatch, grouped GEMM, combine back to back (PDL)"}
+        else:
+            r["roofline"] = {"bound": "tensor", "achieved": tfs, "peak": fp8_burst, "unit": "TFLOP/s",
+                             "frac": tfs / fp8_burst, "frac_of_sustained": tfs / fp8_sust,
+                             "peak_source": f"{fp8_kind} (burst; sustained {fp8_sust:.0f})",
+                             "traffic": None}
+        r["device_status"] = M.moe_device_status()
+        out[name] = r
+        del b, y
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -629,16 +748,27 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dbo", action="store_true")
+    ap.add_argument("--no-gemm", action="store_true")
+    ap.add_argument("--gemm-only", action="store_true", help="only the grouped GEMM measurement")
+    ap.add_argument("--gemm-experts", type=int, default=0, help="with --gemm-only: E experts (profiling case)")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.gemm_only:
+        import torch
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"expert_gemm": run_gemm(args, dev, experts=args.gemm_experts)}), flush=True)
         return
     line, dev = run_ours(args, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_dbo:
             line["dbo"] = run_dbo(args, dev)
             line["dbo_layers"] = run_dbo_layers(args, dev)
+        if world == 1 and not args.no_gemm:
+            line["expert_gemm"] = run_gemm(args, dev)
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(W.WORKLOADS[WORKLOAD])
         print(json.dumps(line), flush=True)

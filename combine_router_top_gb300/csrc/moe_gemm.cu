@@ -8,16 +8,22 @@
 //
 // for r < min(counts[e], C), n < H, blocks b of 128 inputs. q and w are e4m3.
 //
-// One CTA computes a 128 x 128 tile (128 rows of one expert, 128 outputs):
-//   warp 0      one lane issues the TMA loads of the A (rows) and B (weights)
-//               128 x 128-byte tiles, 128-byte swizzled, into a 3-stage ring;
-//   warp 1      allocates 256 TMEM columns; one lane issues, per block b,
-//               four tcgen05.mma kind::f8f6f4 (K = 32 each) into one of two
-//               128-column fp32 accumulators, fresh for every b;
-//   warps 2..9  read the block's accumulator (tcgen05.ld), release it, and add
-//               it times a_scale[r][b] * w_scale[n/128][b] into 64 registers per
-//               thread (two warps per 32-lane TMEM quadrant, 64 columns each);
-//               after the last block they round to bf16 and store the rows.
+// A persistent grid (one CTA per SM) walks the list of 128 x 256 output tiles
+// (128 rows of one expert, 256 outputs) that hold kept rows; each CTA builds
+// that list from counts in shared memory. In each CTA:
+//   warp 0       one lane issues the TMA loads of the A (rows, 128 x 128 B) and
+//                B (weights, 256 x 128 B) tiles, 128-byte swizzled, into a
+//                4-stage ring;
+//   warp 1       allocates all 512 TMEM columns; one lane issues, per block b
+//                of 128 inputs, four tcgen05.mma kind::f8f6f4 (128 x 256 x 32)
+//                into one of two 256-column fp32 accumulators, fresh for every b;
+//   warps 2..17  read the block's accumulator (tcgen05.ld), release it, and add
+//                it times a_scale[r][b] * w_scale[n/128][b] into 64 registers per
+//                thread (four warps per 32-lane TMEM quadrant, 64 columns each);
+//                after a tile's last block they round to bf16 and store its rows
+//                while the tensor cores start on the next tile;
+//   warps 18, 19 idle: registers are granted per four warps, so 20 warps of
+//                96 registers fit where 18 warps of 112 do not.
 // The fp32 scales of both operands change with b, so the per-block partial
 // sums are scaled outside the tensor core (the hardware block-scaled MMA
 // takes power-of-two scales per 32 elements, not these).
@@ -35,13 +41,16 @@
 namespace moe {
 namespace {
 
-constexpr int kGemmTile = 128;                  // rows, outputs and inputs per tile / block
-constexpr int kGemmStages = 3;
-constexpr int kGemmEpiWarps = 8;
-constexpr int kGemmThreads = 32 * (2 + kGemmEpiWarps);
-constexpr uint32_t kGemmTileBytes = kGemmTile * kGemmTile;     // one e4m3 tile: 16 KB
-constexpr uint32_t kGemmStageBytes = 2 * kGemmTileBytes;
-constexpr uint32_t kGemmTmemCols = 2 * kGemmTile;              // two fp32 accumulators
+constexpr int kBM = 128;                         // rows of one expert per tile
+constexpr int kBN = 256;                         // outputs per tile
+constexpr int kBK = 128;                         // inputs per block (one scale per row and block)
+constexpr int kGemmStages = 4;
+constexpr int kGemmEpiWarps = 16;
+constexpr int kGemmThreads = 32 * (2 + kGemmEpiWarps + 2);   // + 2 idle warps: 20 warps, 96 registers each
+constexpr uint32_t kATileBytes = kBM * kBK;      // e4m3: 16 KB
+constexpr uint32_t kBTileBytes = kBN * kBK;      // e4m3: 32 KB
+constexpr uint32_t kGemmStageBytes = kATileBytes + kBTileBytes;
+constexpr uint32_t kGemmTmemCols = 2 * kBN;      // two fp32 accumulators: all 512 columns
 constexpr size_t kGemmSmemBytes = kGemmStages * kGemmStageBytes + 1024;   // + alignment slack
 constexpr unsigned kGemmPollLimit = 1u << 20;
 
@@ -56,11 +65,11 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor: kind::f8f6f4, A and B e4m3, both K-major, fp32
-// accumulator, M = N = 128.
+// accumulator, M = 128, N = 256.
 constexpr uint32_t kIdescF8 = (1u << 4)                          // D format f32
                               | (0u << 7) | (0u << 10)           // A, B e4m3
-                              | ((uint32_t)(kGemmTile >> 3) << 17)   // N / 8
-                              | ((uint32_t)(kGemmTile >> 4) << 24);  // M / 16
+                              | ((uint32_t)(kBN >> 3) << 17)     // N / 8
+                              | ((uint32_t)(kBM >> 4) << 24);    // M / 16
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -111,22 +120,42 @@ __device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, volatil
     return false;
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 2)
+// The tiles holding kept rows, in the order (expert, output tile, row tile):
+// s_first[e] = index of expert e's first tile, s_first[E] = the total.
+struct TileList {
+    const int *first, *kept;
+    int E, n_tiles;
+    __device__ __forceinline__ void decode(int t, int &e, int &nt, int &mt, int &rows) const {
+        int lo = 0, hi = E;                          // first[lo] <= t < first[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (first[mid] <= t) lo = mid; else hi = mid;
+        }
+        e = lo;
+        const int mtiles = (first[e + 1] - first[e]) / n_tiles;
+        const int local = t - first[e];
+        nt = local / mtiles;
+        mt = local - nt * mtiles;
+        rows = min(kept[e] - mt * kBM, kBM);
+    }
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
 expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                        const float *__restrict__ a_scale, const int32_t *__restrict__ counts,
-                       const float *__restrict__ w_scale, uint16_t *__restrict__ y, int H, int C, int n_tiles,
-                       int m_tiles, unsigned *status) {
+                       const float *__restrict__ w_scale, uint16_t *__restrict__ y, int H, int C, int E,
+                       unsigned *status) {
     extern __shared__ uint8_t gemm_smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kGemmStages], empty_bar[kGemmStages];
     __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
+    __shared__ int s_first[kMaxExperts + 1];
+    __shared__ int s_kept[kMaxExperts];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x % m_tiles;
-    const int nt = (blockIdx.x / m_tiles) % n_tiles;
-    const int e = blockIdx.x / (m_tiles * n_tiles);
-    const int nkb = H / kGemmTile;
+    const int nkb = H / kBK, nb = H / 128;
+    const int n_tiles = (H + kBN - 1) / kBN;
     const uint32_t smem0 = (smem_u32(gemm_smem_raw) + 1023u) & ~1023u;
 
     if (threadIdx.x == 0) {
@@ -142,12 +171,34 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
         fence_mbar_init();
     }
     pdl_wait();                                   // counts and the dispatched rows are final from here on
-    const int kept = min(__ldg(counts + e), C);
-    const int rows = min(kept - mt * kGemmTile, kGemmTile);
-    if (rows <= 0) {                              // no row of this expert in this tile
+    if (warp == 0) {                              // tile list: lane l scans experts [l*per, l*per + per)
+        const int per = (E + 31) / 32;
+        int sum = 0;
+        for (int e = lane * per; e < min(E, lane * per + per); ++e) {
+            const int kept = min(__ldg(counts + e), C);
+            s_kept[e] = kept;
+            sum += (kept + kBM - 1) / kBM * n_tiles;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int e = lane * per; e < min(E, lane * per + per); ++e) {
+            s_first[e] = run;
+            run += (s_kept[e] + kBM - 1) / kBM * n_tiles;
+        }
+        if (lane == 31) s_first[E] = incl;
+    }
+    __syncthreads();
+    const int total = s_first[E];
+    if ((int)blockIdx.x >= total) {               // no tile for this CTA
         pdl_launch_dependents();
         return;
     }
+    const TileList tiles{s_first, s_kept, E, n_tiles};
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                      "r"(kGemmTmemCols)
@@ -159,86 +210,100 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    int issued = 0;                               // producer: stages loaded
-    int committed = 0;                            // MMA issuer: blocks committed
+    uint32_t issued = 0;                          // producer: stages loaded
+    uint32_t committed = 0;                       // MMA issuer: blocks committed
     if (warp == 0) {
         if (lane == 0) {
-            const int row_a = e * C + mt * kGemmTile;
-            const int row_b = e * H + nt * kGemmTile;
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % kGemmStages;
-                if (kb >= kGemmStages &&
-                    !gemm_wait(smem_u32(&empty_bar[s]), ((kb / kGemmStages) + 1) & 1, &s_abort))
-                    break;
-                const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kGemmTileBytes;
-                mbar_expect_tx(&full_bar[s], kGemmStageBytes);
-                tma_load_2d(sa, &map_a, smem_u32(&full_bar[s]), kb * kGemmTile, row_a);
-                tma_load_2d(sb, &map_b, smem_u32(&full_bar[s]), kb * kGemmTile, row_b);
-                issued = kb + 1;
+            uint32_t g = 0;
+            for (int t = blockIdx.x; t < total && !s_abort; t += gridDim.x) {
+                int e, nt, mt, rows;
+                tiles.decode(t, e, nt, mt, rows);
+                const int row_a = e * C + mt * kBM;
+                const int row_b = e * H + nt * kBN;
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                    const int s = g % kGemmStages;
+                    if (g >= kGemmStages &&
+                        !gemm_wait(smem_u32(&empty_bar[s]), ((g / kGemmStages) + 1) & 1, &s_abort))
+                        break;
+                    const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kATileBytes;
+                    mbar_expect_tx(&full_bar[s], kGemmStageBytes);
+                    tma_load_2d(sa, &map_a, smem_u32(&full_bar[s]), kb * kBK, row_a);
+                    tma_load_2d(sb, &map_b, smem_u32(&full_bar[s]), kb * kBK, row_b);
+                    issued = g + 1;
+                }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            for (int kb = 0; kb < nkb; ++kb) {
-                const int s = kb % kGemmStages, buf = kb & 1;
-                if (!gemm_wait(smem_u32(&full_bar[s]), (kb / kGemmStages) & 1, &s_abort)) break;
-                if (kb >= 2 && !gemm_wait(smem_u32(&tempty_bar[buf]), ((kb >> 1) + 1) & 1, &s_abort)) break;
-                tc_fence_after();
-                const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kGemmTileBytes;
-                const uint32_t d = tmem + buf * kGemmTile;
+            uint32_t g = 0;
+            for (int t = blockIdx.x; t < total && !s_abort; t += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                    const int s = g % kGemmStages, buf = g & 1;
+                    if (!gemm_wait(smem_u32(&full_bar[s]), (g / kGemmStages) & 1, &s_abort)) break;
+                    if (g >= 2 && !gemm_wait(smem_u32(&tempty_bar[buf]), ((g >> 1) + 1) & 1, &s_abort)) break;
+                    tc_fence_after();
+                    const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kATileBytes;
+                    const uint32_t d = tmem + buf * kBN;
 #pragma unroll
-                for (int k = 0; k < kGemmTile / 32; ++k)
-                    mma_f8(d, umma_desc_sw128(sa + 32 * k), umma_desc_sw128(sb + 32 * k), k > 0 ? 1u : 0u);
-                mma_commit(smem_u32(&empty_bar[s]));
-                mma_commit(smem_u32(&tfull_bar[buf]));
-                committed = kb + 1;
+                    for (int k = 0; k < kBK / 32; ++k)
+                        mma_f8(d, umma_desc_sw128(sa + 32 * k), umma_desc_sw128(sb + 32 * k), k > 0 ? 1u : 0u);
+                    mma_commit(smem_u32(&empty_bar[s]));
+                    mma_commit(smem_u32(&tfull_bar[buf]));
+                    committed = g + 1;
+                }
             }
         }
-    } else {
+    } else if (warp < 2 + kGemmEpiWarps) {
         const int quad = warp & 3;                        // TMEM lanes this warp may read
-        const int half = (warp - 2) >> 2;                 // which 64 of the 128 columns
+        const int cg = (warp - 2) >> 2;                   // which 64 of the 256 columns
         const int r = quad * 32 + lane;                   // row within the tile
-        const bool live = r < rows;
-        const size_t grow = (size_t)e * C + (size_t)mt * kGemmTile + r;
-        const float *sa_row = a_scale + grow * nkb;
-        const float *sw_row = w_scale + ((size_t)e * n_tiles + nt) * nkb;
-        float acc[64];
-#pragma unroll
-        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
-        float f_next = live ? __ldg(sa_row) * __ldg(sw_row) : 0.0f;
+        uint32_t g = 0;
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int buf = kb & 1;
-            const float f = f_next;
-            if (kb + 1 < nkb) f_next = live ? __ldg(sa_row + kb + 1) * __ldg(sw_row + kb + 1) : 0.0f;
-            int got = 0;
-            if (lane == 0) got = gemm_wait(smem_u32(&tfull_bar[buf]), (kb >> 1) & 1, &s_abort) ? 1 : 0;
-            if (!__shfl_sync(kFull, got, 0)) {
-                ok = false;
-                break;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            int e, nt, mt, rows;
+            tiles.decode(t, e, nt, mt, rows);
+            const int nblk = nt * (kBN / 128) + (cg >> 1);    // 128-output block of this warp's columns
+            const bool live = r < rows && nblk < nb;
+            const size_t grow = (size_t)e * C + (size_t)mt * kBM + r;
+            const float *sa_row = a_scale + grow * nb;
+            const float *sw_row = w_scale + ((size_t)e * nb + (live ? nblk : 0)) * nb;
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            float f_next = live ? __ldg(sa_row) * __ldg(sw_row) : 0.0f;
+            for (int kb = 0; kb < nkb; ++kb, ++g) {
+                const int buf = g & 1;
+                const float f = f_next;
+                if (kb + 1 < nkb) f_next = live ? __ldg(sa_row + kb + 1) * __ldg(sw_row + kb + 1) : 0.0f;
+                int got = 0;
+                if (lane == 0) got = gemm_wait(smem_u32(&tfull_bar[buf]), (g >> 1) & 1, &s_abort) ? 1 : 0;
+                if (!__shfl_sync(kFull, got, 0)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * kBN + cg * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {                // 16 columns at a time: 64 + 16 live values
+                    uint32_t v[16];
+                    tmem_ld16(taddr + 16 * c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(__uint_as_float(v[j]), f, acc[c * 16 + j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
             }
-            tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * kGemmTile + half * 64;
-            uint32_t v[4][16];
-            tmem_ld16(taddr + 0, v[0]);
-            tmem_ld16(taddr + 16, v[1]);
-            tmem_ld16(taddr + 32, v[2]);
-            tmem_ld16(taddr + 48, v[3]);
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+            if (ok && live) {
+                uint4 *dst = reinterpret_cast<uint4 *>(y + grow * H + (size_t)nt * kBN + cg * 64);
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int j = 0; j < 16; ++j) acc[c * 16 + j] = fmaf(__uint_as_float(v[c][j]), f, acc[c * 16 + j]);
-        }
-        if (ok && live) {
-            uint4 *dst = reinterpret_cast<uint4 *>(y + grow * H + (size_t)nt * kGemmTile + half * 64);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                dst[c] = make_uint4(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
-                                    pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+                for (int c = 0; c < 8; ++c)
+                    dst[c] = make_uint4(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1]),
+                                        pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                                        pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]),
+                                        pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+            }
         }
     }
     pdl_launch_dependents();
@@ -250,8 +315,8 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
         volatile int no_abort = 0;
         if (warp == 0 && lane == 0) {
             atomicOr(status, kStatusWaitGaveUp);
-            for (int kb = (issued > kGemmStages ? issued - kGemmStages : 0); kb < issued; ++kb)
-                gemm_wait(smem_u32(&full_bar[kb % kGemmStages]), (kb / kGemmStages) & 1, &no_abort);
+            for (uint32_t g = (issued > kGemmStages ? issued - kGemmStages : 0); g < issued; ++g)
+                gemm_wait(smem_u32(&full_bar[g % kGemmStages]), (g / kGemmStages) & 1, &no_abort);
         }
         if (warp == 1 && lane == 0 && committed > 0)
             gemm_wait(smem_u32(&tfull_bar[(committed - 1) & 1]), ((committed - 1) >> 1) & 1, &no_abort);
@@ -280,14 +345,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// A [rows][cols] byte matrix read in 128 x 128 tiles, 128-byte swizzled;
-// rows past the end read as zero.
-bool encode_tile_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols) {
+// A [rows][cols] byte matrix read in tiles of box_rows x 128 bytes, 128-byte
+// swizzled; rows past the end read as zero.
+bool encode_tile_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols};
-    const cuuint32_t box[2] = {kGemmTile, kGemmTile};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -310,8 +375,8 @@ extern "C" int moe_expert_gemm_fp8(const moe_problem *p, const void *recv_q, con
         !aligned(w_scale, 4) || !aligned(counts, 4))
         return MOE_ERR_INVALID_ARG;
     CUtensorMap map_a, map_b;
-    if (!encode_tile_map(&map_a, recv_q, (uint64_t)d.E * d.C, (uint64_t)d.H) ||
-        !encode_tile_map(&map_b, w_q, (uint64_t)d.E * d.H, (uint64_t)d.H))
+    if (!encode_tile_map(&map_a, recv_q, (uint64_t)d.E * d.C, (uint64_t)d.H, kBM) ||
+        !encode_tile_map(&map_b, w_q, (uint64_t)d.E * d.H, (uint64_t)d.H, kBN))
         return MOE_ERR_CUDA;
     unsigned *status = device_status_word();
     if (status == nullptr) return MOE_ERR_CUDA;
@@ -324,13 +389,11 @@ extern "C" int moe_expert_gemm_fp8(const moe_problem *p, const void *recv_q, con
             return MOE_ERR_CUDA;
         smem_set[dev] = true;
     }
-    const int n_tiles = d.H / kGemmTile;
-    const int m_tiles = (d.C + kGemmTile - 1) / kGemmTile;
-    const long long grid = (long long)d.E * n_tiles * m_tiles;
-    if (grid > 0x7FFFFFFFLL) return MOE_ERR_UNSUPPORTED;
-    if (launch_pdl_smem(expert_gemm_fp8_kernel, (int)grid, kGemmThreads, kGemmSmemBytes, as_stream(stream), map_a,
-                        map_b, recv_scale, counts, w_scale, static_cast<uint16_t *>(y), d.H, d.C, n_tiles, m_tiles,
-                        status) != cudaSuccess)
+    int grid = sm_count();                        // persistent: one CTA per SM
+    if (d.max_blocks > 0 && d.max_blocks < grid) grid = d.max_blocks;
+    if (launch_pdl_smem(expert_gemm_fp8_kernel, grid, kGemmThreads, kGemmSmemBytes, as_stream(stream), map_a, map_b,
+                        recv_scale, counts, w_scale, static_cast<uint16_t *>(y), d.H, d.C, d.E, status) !=
+        cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
