@@ -438,6 +438,42 @@ def run_ours(args, rank: int, world: int, local: int):
     fused_ms = reduce_max(statistics.fmean(a.elapsed_time(z) for a, z in evf), world, dev)
     fused_pipe_ms = reduce_max(statistics.fmean(a.elapsed_time(z) for a, z in evfp), world, dev)
     assert torch.equal(out, out_ref), "fused route+dispatch changed the step's output"
+
+    # expert + combine with per-row readiness (one cooperative kernel) against
+    # the two calls chained by PDL; L2 flushed before each pair
+    epoch = [0]
+
+    def ready_pair():
+        epoch[0] += 1
+        M.moe_expert_combine(p, b["recv"], b.get("recv_scale"), b["counts"], s, b["y"], b["topk_idx"],
+                             b["topk_w"], b["slot"], out, b["ready_flags"], epoch[0], stream)
+
+    def separate_pair():
+        calls[2][1]()
+        calls[3][1]()
+    for _ in range(3):
+        flush()
+        ready_pair()
+    evr = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+           for n in ("ready", "separate", "ready_step")}
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    for i in range(K):
+        for n, fn in (("ready", ready_pair), ("separate", separate_pair)):
+            flush()
+            evr[n][i][0].record(stream)
+            fn()
+            evr[n][i][1].record(stream)
+        flush()
+        evr["ready_step"][i][0].record(stream)
+        calls[0][1]()
+        calls[1][1]()
+        ready_pair()
+        evr["ready_step"][i][1].record(stream)
+    torch.cuda.synchronize()
+    ready_ms = {n: reduce_max(statistics.fmean(a.elapsed_time(z) for a, z in v), world, dev) for n, v in evr.items()}
+    assert torch.equal(out, out_ref), "expert+combine with readiness flags changed the step's output"
+    assert M.moe_device_status() == M.MOE_OK
     step_ms = sum(ms.values())
     dc_ms = reduce_max(ms["dispatch"] + ms["combine"], world, dev)
     step_ms_max = reduce_max(step_ms, world, dev)
@@ -546,6 +582,12 @@ def run_ours(args, rank: int, world: int, local: int):
                 "pipelined_ms_per_step": fused_pipe_ms, "pipelined_tokens_per_s": world * w.T / (fused_pipe_ms * 1e-3),
                 "what": "moe_route_dispatch (top-k kernel, then one kernel that forms slots and dispatches), "
                         "L2 flushed before each call; pipelined: fused call, expert, combine"},
+            "expert_combine_ready": {
+                "us": 1e3 * ready_ms["ready"], "separate_us": 1e3 * ready_ms["separate"],
+                "step_ms": ready_ms["ready_step"], "step_tokens_per_s": world * w.T / (ready_ms["ready_step"] * 1e-3),
+                "what": "moe_expert_combine (one cooperative kernel, readiness per expert row) against "
+                        "moe_expert_synthetic + moe_combine chained by PDL, L2 flushed before each pair; "
+                        "step: route, dispatch, moe_expert_combine"},
         }
     return line, dev
 

@@ -80,6 +80,8 @@ def lib() -> C.CDLL:
             "moe_route_dispatch": ([pp, P, P, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
             "moe_expert_synthetic": ([pp, P, P, P, P, P, P], i),
             "moe_expert_gemm_fp8": ([pp, P, P, P, P, P, P, P], i),
+            "moe_ready_flags_bytes": ([pp], C.c_size_t),
+            "moe_expert_combine": ([pp, P, P, P, P, P, P, P, P, P, P, C.c_size_t, C.c_uint32, P], i),
             "moe_combine": ([pp, P, P, P, P, P, P], i),
             "dbo_create": ([C.POINTER(P)], i),
             "dbo_destroy": ([P], None),
@@ -99,7 +101,8 @@ def lib() -> C.CDLL:
 
 EXPORTS = ("moe_status_string", "moe_validate", "moe_device_status", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
            "moe_dispatch", "moe_route_dispatch_workspace_bytes", "moe_route_dispatch",
-           "moe_expert_synthetic", "moe_expert_gemm_fp8", "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
+           "moe_expert_synthetic", "moe_expert_gemm_fp8", "moe_ready_flags_bytes", "moe_expert_combine",
+           "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
            "moe_layer_stand_in", "dbo_layers", "dbo_layers_capture", "dbo_graph_launch")
 
 
@@ -196,6 +199,19 @@ def moe_expert_gemm_fp8(p, recv_q, recv_scale, counts, w_q, w_scale, y, stream=N
     _check("moe_expert_gemm_fp8", rc)
 
 
+def moe_ready_flags_bytes(p: moe_problem) -> int:
+    return lib().moe_ready_flags_bytes(C.byref(p))
+
+
+def moe_expert_combine(p, recv, recv_scale, counts, s, y, topk_idx, topk_w, slot, out, flags, epoch: int,
+                       stream=None):
+    """Synthetic expert + combine in one kernel with per-row readiness flags (epoch: nonzero, fresh per call)."""
+    rc = lib().moe_expert_combine(C.byref(p), _ptr(recv), _ptr(recv_scale), _ptr(counts), _ptr(s), _ptr(y),
+                                  _ptr(topk_idx), _ptr(topk_w), _ptr(slot), _ptr(out), _ptr(flags),
+                                  flags.numel() * flags.element_size(), epoch, _stream(stream))
+    _check("moe_expert_combine", rc)
+
+
 def moe_combine(p, y, topk_idx, topk_w, slot, out, stream=None):
     rc = lib().moe_combine(C.byref(p), _ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(slot), _ptr(out),
                            _stream(stream))
@@ -273,6 +289,8 @@ def alloc_buffers(p: moe_problem, device="cuda") -> dict:
         "recv_src": torch.empty((E, Cap), **i32),
         "y": torch.empty((E, Cap, H), dtype=torch.int16, device=device),
         "workspace": torch.empty(ws, dtype=torch.uint8, device=device),
+        # per-row readiness flags of moe_expert_combine: zero-filled once, then epoch-tagged
+        "ready_flags": torch.zeros(max(moe_ready_flags_bytes(p) // 4, 1), **i32),
     }
     return b
 

@@ -177,6 +177,54 @@ __device__ __forceinline__ void pdl_enter() {
     pdl_launch_dependents();
 }
 
+// Exclusive scan of min(counts[e], C) over e into off[0..E] (off[E] = kept rows).
+__device__ __forceinline__ void kept_row_offsets(const int32_t *__restrict__ counts, int E, int C, int32_t *off, int32_t *warp_tot) {
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (E + nt - 1) / nt;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) {
+        const int c = __ldg(counts + e);
+        local += c < C ? c : C;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < (nt >> 5) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += n;
+        }
+        warp_tot[lane] = v;
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int e = e0; e < e1; ++e) {
+        off[e] = run;
+        const int c = __ldg(counts + e);
+        run += c < C ? c : C;
+    }
+    if (tid == nt - 1) off[E] = run;
+    __syncthreads();
+}
+
+// Expert of kept row p: the last e with off[e] <= p (off is non-decreasing).
+__device__ __forceinline__ int expert_of_row(const int32_t *off, int E, int p) {
+    int lo = 0, hi = E;        // off[lo] <= p < off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= p) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
 // Walks the work units unit0, unit0 + stride, ... of a (row, segment) grid
 // with `segs` segments per row, keeping (row, seg) without any division in
 // the loop.

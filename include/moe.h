@@ -221,6 +221,30 @@ int moe_expert_gemm_fp8(const moe_problem *p, const void *recv_q, const float *r
                         const int32_t *counts, const void *w_q, const float *w_scale,
                         void *y, void *stream);
 
+/* Synthetic expert and combine in one kernel, readiness tracked per expert
+ * row instead of per kernel: [PMC §Further Improvements] notes that buffers
+ * shared across devices allow synchronisation per token instead of per batch.
+ * Every warp first computes its units of y (kept row, segment of 32 x 4
+ * sixteen-byte input pieces; the arithmetic of moe_expert_synthetic) and
+ * publishes each with a release store of `epoch` into its flag, then combines
+ * tokens in order (the arithmetic of moe_combine), each unit once the flags
+ * of the row segments it reads hold `epoch`. y and out come out bit for bit
+ * as moe_expert_synthetic followed by moe_combine write them.
+ * flags: device u32[E*C*segments] (moe_ready_flags_bytes(p) bytes), owned by the
+ * caller, zero-filled before first use, not shared with a concurrent call.
+ * epoch: nonzero, never repeated since the flags were last zero-filled (an
+ * incrementing counter). The grid is launched cooperatively (all blocks
+ * resident; not a programmatic dependent); max_blocks caps it (>= 2).
+ * A consumer wait that gives up after 100 ms (inputs inconsistent with counts)
+ * raises the device status word (moe_device_status: MOE_ERR_TIMEOUT) and that
+ * unit of out is not written. */
+size_t moe_ready_flags_bytes(const moe_problem *p);
+int moe_expert_combine(const moe_problem *p, const void *recv, const float *recv_scale,
+                       const int32_t *counts, const float *s, void *y,
+                       const int32_t *topk_idx, const float *topk_w, const int32_t *slot,
+                       void *out, uint32_t *flags, size_t flags_bytes, uint32_t epoch,
+                       void *stream);
+
 /* Step 4: combine. [PMC §Combine]: the expert outputs are read back through
  * the routing table and summed with the router weights into an externally
  * allocated tensor:

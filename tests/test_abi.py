@@ -117,6 +117,31 @@ def test_gemm_rejects_bad_arguments_before_any_launch(moe):
         assert L.moe_expert_gemm_fp8(C.byref(p), *a, None) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_expert_combine_rejects_bad_arguments_before_any_launch(moe):
+    L = moe.lib()
+    p = mk(moe)
+    assert moe.moe_ready_flags_bytes(p) == 256 * 128 * 4 * 4        # 448 fp8 pieces per row: 4 segments of 128
+    assert moe.moe_ready_flags_bytes(mk(moe, dtype=0)) == 256 * 128 * 7 * 4   # 896 bf16 pieces: 7 segments
+    assert moe.moe_ready_flags_bytes(mk(moe, k=0)) == 0
+    fake = C.c_void_p(1 << 40)
+    args = [fake] * 9
+    fb = 256 * 128 * 4 * 4
+    # epoch 0, flags too small, missing flags
+    assert L.moe_expert_combine(C.byref(p), *args, fake, fb, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_expert_combine(C.byref(p), *args, fake, fb - 4, 1, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_expert_combine(C.byref(p), *args, None, fb, 1, None) == moe.MOE_ERR_INVALID_ARG
+    # fp8 needs recv_scale
+    a = list(args)
+    a[1] = None
+    assert L.moe_expert_combine(C.byref(p), *a, fake, fb, 1, None) == moe.MOE_ERR_INVALID_ARG
+    # misaligned y
+    a = list(args)
+    a[4] = C.c_void_p((1 << 40) + 8)
+    assert L.moe_expert_combine(C.byref(p), *a, fake, fb, 1, None) == moe.MOE_ERR_INVALID_ARG
+    # empty batch: nothing to do
+    assert L.moe_expert_combine(C.byref(mk(moe, T=0)), *args, fake, fb, 1, None) == moe.MOE_OK
+
+
 def test_calls_reject_bad_arguments_before_any_launch(moe):
     L = moe.lib()
     p = mk(moe)
