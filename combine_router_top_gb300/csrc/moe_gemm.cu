@@ -42,15 +42,17 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;                         // rows of one expert per tile
-constexpr int kBN = 256;                         // outputs per tile
+constexpr int kBN = 256;                         // outputs per tile (128 or 256)
 constexpr int kBK = 128;                         // inputs per block (one scale per row and block)
-constexpr int kGemmStages = 4;
+constexpr int kNumAcc = 512 / kBN;               // fp32 accumulators that fill the 512 TMEM columns
+constexpr int kGemmStages = (196 * 1024) / (kBM * kBK + kBN * kBK);
 constexpr int kGemmEpiWarps = 16;
 constexpr int kGemmThreads = 32 * (2 + kGemmEpiWarps + 2);   // + 2 idle warps: 20 warps, 96 registers each
 constexpr uint32_t kATileBytes = kBM * kBK;      // e4m3: 16 KB
 constexpr uint32_t kBTileBytes = kBN * kBK;      // e4m3: 32 KB
 constexpr uint32_t kGemmStageBytes = kATileBytes + kBTileBytes;
-constexpr uint32_t kGemmTmemCols = 2 * kBN;      // two fp32 accumulators: all 512 columns
+constexpr uint32_t kGemmTmemCols = kNumAcc * kBN;   // all 512 columns
+constexpr int kEpiCols = kBN / 4;                // columns per promotion warp (4 per TMEM lane quadrant)
 constexpr size_t kGemmSmemBytes = kGemmStages * kGemmStageBytes + 1024;   // + alignment slack
 constexpr unsigned kGemmPollLimit = 1u << 20;
 
@@ -147,7 +149,7 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                        unsigned *status) {
     extern __shared__ uint8_t gemm_smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kGemmStages], empty_bar[kGemmStages];
-    __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2];
+    __shared__ __align__(8) uint64_t tfull_bar[kNumAcc], tempty_bar[kNumAcc];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     __shared__ int s_first[kMaxExperts + 1];
@@ -163,7 +165,7 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kNumAcc; ++b) {
             mbar_init(&tfull_bar[b], 1);
             mbar_init(&tempty_bar[b], kGemmEpiWarps);
         }
@@ -238,9 +240,11 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
             uint32_t g = 0;
             for (int t = blockIdx.x; t < total && !s_abort; t += gridDim.x) {
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
-                    const int s = g % kGemmStages, buf = g & 1;
+                    const int s = g % kGemmStages, buf = g % kNumAcc;
                     if (!gemm_wait(smem_u32(&full_bar[s]), (g / kGemmStages) & 1, &s_abort)) break;
-                    if (g >= 2 && !gemm_wait(smem_u32(&tempty_bar[buf]), ((g >> 1) + 1) & 1, &s_abort)) break;
+                    if (g >= kNumAcc &&
+                        !gemm_wait(smem_u32(&tempty_bar[buf]), ((g / kNumAcc) + 1) & 1, &s_abort))
+                        break;
                     tc_fence_after();
                     const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kATileBytes;
                     const uint32_t d = tmem + buf * kBN;
@@ -255,36 +259,36 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
         }
     } else if (warp < 2 + kGemmEpiWarps) {
         const int quad = warp & 3;                        // TMEM lanes this warp may read
-        const int cg = (warp - 2) >> 2;                   // which 64 of the 256 columns
+        const int cg = (warp - 2) >> 2;                   // which quarter of the tile's columns
         const int r = quad * 32 + lane;                   // row within the tile
         uint32_t g = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             int e, nt, mt, rows;
             tiles.decode(t, e, nt, mt, rows);
-            const int nblk = nt * (kBN / 128) + (cg >> 1);    // 128-output block of this warp's columns
+            const int nblk = (nt * kBN + cg * kEpiCols) / 128;   // 128-output block of this warp's columns
             const bool live = r < rows && nblk < nb;
             const size_t grow = (size_t)e * C + (size_t)mt * kBM + r;
             const float *sa_row = a_scale + grow * nb;
             const float *sw_row = w_scale + ((size_t)e * nb + (live ? nblk : 0)) * nb;
-            float acc[64];
+            float acc[kEpiCols];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            for (int j = 0; j < kEpiCols; ++j) acc[j] = 0.0f;
             float f_next = live ? __ldg(sa_row) * __ldg(sw_row) : 0.0f;
             for (int kb = 0; kb < nkb; ++kb, ++g) {
-                const int buf = g & 1;
+                const int buf = g % kNumAcc;
                 const float f = f_next;
                 if (kb + 1 < nkb) f_next = live ? __ldg(sa_row + kb + 1) * __ldg(sw_row + kb + 1) : 0.0f;
                 int got = 0;
-                if (lane == 0) got = gemm_wait(smem_u32(&tfull_bar[buf]), (g >> 1) & 1, &s_abort) ? 1 : 0;
+                if (lane == 0) got = gemm_wait(smem_u32(&tfull_bar[buf]), (g / kNumAcc) & 1, &s_abort) ? 1 : 0;
                 if (!__shfl_sync(kFull, got, 0)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * kBN + cg * 64;
+                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * kBN + cg * kEpiCols;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {                // 16 columns at a time: 64 + 16 live values
+                for (int c = 0; c < kEpiCols / 16; ++c) {     // 16 columns at a time
                     uint32_t v[16];
                     tmem_ld16(taddr + 16 * c, v);
                     tmem_ld_wait();
@@ -296,9 +300,9 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                 if (lane == 0) mbar_arrive(&tempty_bar[buf]);
             }
             if (ok && live) {
-                uint4 *dst = reinterpret_cast<uint4 *>(y + grow * H + (size_t)nt * kBN + cg * 64);
+                uint4 *dst = reinterpret_cast<uint4 *>(y + grow * H + (size_t)nt * kBN + cg * kEpiCols);
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
+                for (int c = 0; c < kEpiCols / 8; ++c)
                     dst[c] = make_uint4(pack_bf16x2(acc[8 * c + 0], acc[8 * c + 1]),
                                         pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
                                         pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]),
@@ -319,7 +323,7 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                 gemm_wait(smem_u32(&full_bar[g % kGemmStages]), (g / kGemmStages) & 1, &no_abort);
         }
         if (warp == 1 && lane == 0 && committed > 0)
-            gemm_wait(smem_u32(&tfull_bar[(committed - 1) & 1]), ((committed - 1) >> 1) & 1, &no_abort);
+            gemm_wait(smem_u32(&tfull_bar[(committed - 1) % kNumAcc]), ((committed - 1) / kNumAcc) & 1, &no_abort);
         __syncthreads();
     }
     if (warp == 1) {
