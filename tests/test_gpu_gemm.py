@@ -126,13 +126,15 @@ def test_gemm_matches_oracle(case):
     print(f"{case}: max |err| / S = {worst:.3g}")
 
 
-def test_gemm_dsv3_full_size_sampled_rows():
-    """DeepSeek-V3 decode shape (1024 tokens, H 7168, 256 experts, C 128): the
-    whole chain route -> dispatch -> GEMM on the GPU, 13 GB of device-drawn
-    weights; sampled rows against the oracle's row entry fed by the oracle's
-    own dispatch; every row past a count untouched."""
+@pytest.mark.parametrize("name", ["dsv3_decode", "dsv3_prefill"])
+def test_gemm_full_size_sampled_rows(name):
+    """The two shapes the benchmark times: DeepSeek-V3 decode (1024 tokens, H
+    7168, 256 experts, C 128) and an 8192-token prefill (C 1024: several row
+    tiles per expert). The whole chain route -> dispatch -> GEMM on the GPU,
+    13 GB of device-drawn weights; sampled rows against the oracle's row entry
+    fed by the oracle's own dispatch; every row past a count untouched."""
     import combine_router_top_gb300 as M
-    w = W.WORKLOADS["dsv3_fp8"]
+    w = W.WORKLOADS["dsv3_fp8"] if name == "dsv3_decode" else W.WORKLOADS["dbo"].with_(dtype=W.DTYPE_FP8_E4M3_B128)
     rq, rs, counts = oracle_dispatch(w)
     p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
     b = M.alloc_buffers(p, DEV)
@@ -154,9 +156,12 @@ def test_gemm_dsv3_full_size_sampled_rows():
     live = [e for e in range(w.E) if kept[e] > 0]
     picks = [(live[0], 0), (live[0], kept[live[0]] - 1), (live[len(live) // 2], 1 % kept[live[len(live) // 2]]),
              (live[-1], kept[live[-1]] - 1), (live[-1], 0), (live[len(live) // 3], kept[live[len(live) // 3]] // 2)]
+    if name == "dsv3_prefill":                     # rows in the second and last row tiles
+        e = int(np.argmax(kept))
+        picks = [(e, 128), (e, kept[e] - 1), (live[1], min(200, kept[live[1]] - 1))] + picks[:3]
     worst = 0.0
     for e, r in picks:
         wq_e, ws_e = wq[e].cpu().numpy(), ws[e].cpu().numpy()
         ref = O.gemm_fp8_row(rq[e, r], rs[e, r], wq_e, ws_e)
         worst = max(worst, check_row(yh[e, r], ref, abs_bound_row(rq[e, r], rs[e, r], wq_e, ws_e)))
-    print(f"dsv3 sampled rows: max |err| / S = {worst:.3g}")
+    print(f"{name} sampled rows: max |err| / S = {worst:.3g}")

@@ -364,6 +364,37 @@ def test_dbo_layers_graph_replay_equals_eager():
     ctx.close()
 
 
+def test_dbo_layers_full_size_as_benchmarked():
+    """The 8192-token dual-batch workload in the configuration the benchmark
+    times (4 layers, 256 busy FMAs per 8 elements): two streams eager, graph
+    replay and the sequential one-stream run agree bit for bit. (The oracle
+    pins the same kernels at this size through the dual-batch step test and
+    the layer schedule at smaller sizes.)"""
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_host
+    w = W.WORKLOADS["dbo"]
+    L, alpha, sigma = 4, 0.75, 1.5
+    x, lg, s, t, bufs, args = _layers_setup(w, L, alpha, sigma, 256)
+    comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    comp.wait_stream(torch.cuda.current_stream())
+    ctx = M.dbo_create()
+    M.dbo_layers(ctx, args, comp, comm)
+    torch.cuda.synchronize()
+    got, got_sh = to_host(t["out"], np.uint16).copy(), to_host(t["shared"], np.uint16).copy()
+    M.dbo_layers_capture(ctx, args, comp, comm)
+    t["out"].fill_(0)
+    torch.cuda.synchronize()
+    M.dbo_graph_launch(ctx, comp)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(t["out"], np.uint16), got)
+    ref, ref_sh = _layers_sequential(w, L, alpha, sigma, t)
+    assert np.array_equal(got, to_host(ref, np.uint16))
+    assert np.array_equal(got_sh, to_host(ref_sh, np.uint16))
+    assert np.isfinite(torch.from_numpy(got.view(np.int16)).view(torch.bfloat16).float().numpy()).all()
+    ctx.close()
+
+
 def test_layer_stand_in_is_exact():
     import torch
     import combine_router_top_gb300 as M
