@@ -479,59 +479,43 @@ def run_ours(args, rank: int, world: int, local: int):
     step_ms_max = reduce_max(step_ms, world, dev)
     comb_ms = reduce_max(ms["combine"], world, dev)
 
-    # end to end through the public API: pinned host in, pinned host out, every
-    # step. Serial: copy in, the four calls, copy out, one after another.
-    # Pipelined (a serving loop): two buffer sets; step i+1's inputs are copied
-    # in and step i-1's output copied out while step i computes.
+    # end to end through the C ABI with host buffers (moe_path_host): every
+    # step copies x and logits in from pinned host memory, runs the four calls
+    # and copies out back to pinned host memory, all issued by one call.
+    # Serial: one stream, one buffer set. Pipelined (a serving loop): three
+    # streams with a buffer set each, used in turn, so that one step's copy in,
+    # another's kernels and a third's copy out run at the same time (each
+    # stream keeps its own step's three phases in order).
+    E2E_SETS = 3
     sets = []
-    for _ in range(2):
+    for _ in range(E2E_SETS):
         sets.append({"x": torch.empty_like(x), "lg": torch.empty_like(lg), "out": torch.empty_like(out),
                      "b": M.alloc_buffers(p, dev),
                      "xp": torch.from_numpy(x_h.view(np.int16)).pin_memory(),
                      "lp": torch.from_numpy(lg_h).pin_memory(),
                      "op": torch.empty((w.T, w.H), dtype=torch.int16).pin_memory()})
-    s_in, s_comp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
-
-    def e2e_serial_step(z):
-        z["x"].copy_(z["xp"], non_blocking=True)
-        z["lg"].copy_(z["lp"], non_blocking=True)
-        M.run_path(p, z["x"], z["lg"], s, z["b"], z["out"], stream)
-        z["op"].copy_(z["out"], non_blocking=True)
+    e2e_streams = [torch.cuda.Stream(device=dev) for _ in range(E2E_SETS)]
+    paths = [M.HostPath(p, z["xp"], z["lp"], s, z["x"], z["lg"], z["b"], z["out"], z["op"], e2e_streams[j])
+             for j, z in enumerate(sets)]
+    serial_path = M.HostPath(p, sets[0]["xp"], sets[0]["lp"], s, sets[0]["x"], sets[0]["lg"], sets[0]["b"],
+                             sets[0]["out"], sets[0]["op"], stream)
 
     def e2e_run(n, pipelined):
-        ev = {key: [torch.cuda.Event() for _ in range(2)] for key in ("in", "comp", "out")}
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world, dev)
         torch.cuda.synchronize()
         e0.record(stream)
         if not pipelined:
             for i in range(n):
-                e2e_serial_step(sets[0])
-            e1.record(stream)
+                serial_path()
         else:
-            for st_ in (s_in, s_comp, s_out):
+            for st_ in e2e_streams:
                 st_.wait_stream(stream)
             for i in range(n):
-                z, j = sets[i % 2], i % 2
-                if i >= 2:
-                    s_in.wait_event(ev["comp"][j])          # set j's previous step has read its inputs
-                with torch.cuda.stream(s_in):
-                    z["x"].copy_(z["xp"], non_blocking=True)
-                    z["lg"].copy_(z["lp"], non_blocking=True)
-                ev["in"][j].record(s_in)
-                s_comp.wait_event(ev["in"][j])
-                if i >= 2:
-                    s_comp.wait_event(ev["out"][j])         # set j's previous output has been copied out
-                M.run_path(p, z["x"], z["lg"], s, z["b"], z["out"], s_comp)
-                ev["comp"][j].record(s_comp)
-                s_out.wait_event(ev["comp"][j])
-                with torch.cuda.stream(s_out):
-                    z["op"].copy_(z["out"], non_blocking=True)
-                ev["out"][j].record(s_out)
-            stream.wait_stream(s_out)
-            stream.wait_stream(s_comp)
-            stream.wait_stream(s_in)
-            e1.record(stream)
+                paths[i % E2E_SETS]()
+            for st_ in e2e_streams:
+                stream.wait_stream(st_)
+        e1.record(stream)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
 
@@ -566,8 +550,9 @@ def run_ours(args, rank: int, world: int, local: int):
             "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": x.numel() * 2 + lg.numel() * 4, "d2h_bytes_per_step": out.numel() * 2,
                     "ms_per_step": e2e_ms,
-                    "what": "every step: H2D x+logits from pinned host, route, dispatch, expert, combine, D2H out "
-                            "to pinned host; two buffer sets, copies of neighbouring steps overlap the compute",
+                    "what": "every step one moe_path_host call: H2D x+logits from pinned host, route, dispatch, "
+                            "expert, combine, D2H out to pinned host; three streams with a buffer set each, used "
+                            "in turn, so that copies of neighbouring steps overlap the compute",
                     "serial_ms_per_step": e2e_serial_ms,
                     "serial_value": world * w.T / (e2e_serial_ms * 1e-3)},
             "gpu_launches": 2 * KERNELS_PER_STEP * K,

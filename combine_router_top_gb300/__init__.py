@@ -81,6 +81,7 @@ def lib() -> C.CDLL:
             "moe_expert_synthetic": ([pp, P, P, P, P, P, P], i),
             "moe_expert_gemm_fp8": ([pp, P, P, P, P, P, P, P], i),
             "moe_ready_flags_bytes": ([pp], C.c_size_t),
+            "moe_path_host": ([pp, P, P, P, P, P, C.POINTER(moe_ubatch_bufs), P, P, P], i),
             "moe_expert_combine": ([pp, P, P, P, P, P, P, P, P, P, P, C.c_size_t, C.c_uint32, P], i),
             "moe_combine": ([pp, P, P, P, P, P, P], i),
             "dbo_create": ([C.POINTER(P)], i),
@@ -101,7 +102,7 @@ def lib() -> C.CDLL:
 
 EXPORTS = ("moe_status_string", "moe_validate", "moe_device_status", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
            "moe_dispatch", "moe_route_dispatch_workspace_bytes", "moe_route_dispatch",
-           "moe_expert_synthetic", "moe_expert_gemm_fp8", "moe_ready_flags_bytes", "moe_expert_combine",
+           "moe_expert_synthetic", "moe_expert_gemm_fp8", "moe_ready_flags_bytes", "moe_expert_combine", "moe_path_host",
            "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
            "moe_layer_stand_in", "dbo_layers", "dbo_layers_capture", "dbo_graph_launch")
 
@@ -252,6 +253,36 @@ def ubatch_bufs(b: dict) -> moe_ubatch_bufs:
                            _ptr(b["slot"]), _ptr(b["rank_counts"]), _ptr(b["dropped"]), _ptr(b["recv"]),
                            _ptr(b.get("recv_scale")), _ptr(b["recv_src"]), _ptr(b["y"]), _ptr(b["workspace"]),
                            b["workspace"].numel() * b["workspace"].element_size())
+
+
+def _host_ptr(t):
+    if t.is_cuda:
+        raise ValueError("moe_path_host takes host tensors for x_host, logits_host and out_host")
+    if not t.is_contiguous():
+        raise ValueError("libmoe_gb300 takes contiguous tensors only")
+    return t.data_ptr()
+
+
+class HostPath:
+    """moe_path_host with its arguments marshalled once: every call() issues
+    one batch (H2D of x and logits, the four stages, D2H of out) on `stream`."""
+
+    def __init__(self, p: moe_problem, x_host, logits_host, s, x_dev, logits_dev, bufs: dict, out_dev, out_host,
+                 stream=None):
+        self.p = p
+        self.ub = ubatch_bufs(bufs)
+        self.args = (C.byref(self.p), _host_ptr(x_host), _host_ptr(logits_host), _ptr(s), _ptr(x_dev),
+                     _ptr(logits_dev), C.byref(self.ub), _ptr(out_dev), _host_ptr(out_host), _stream(stream))
+        self.fn = lib().moe_path_host
+        self._keep = (x_host, logits_host, s, x_dev, logits_dev, bufs, out_dev, out_host)
+
+    def __call__(self):
+        _check("moe_path_host", self.fn(*self.args))
+
+
+def moe_path_host(p, x_host, logits_host, s, x_dev, logits_dev, bufs: dict, out_dev, out_host, stream=None):
+    """The whole path with host inputs and output, in one call (asynchronous on `stream`)."""
+    HostPath(p, x_host, logits_host, s, x_dev, logits_dev, bufs, out_dev, out_host, stream)()
 
 
 def dbo_step(ctx: DboContext, p_full, x, logits, s, bufs2, out, compute_stream, comm_stream, record_timing=False):

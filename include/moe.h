@@ -274,6 +274,23 @@ typedef struct moe_ubatch_bufs {
     size_t workspace_bytes;
 } moe_ubatch_bufs;
 
+/* The whole path for one batch whose inputs and output live in HOST memory,
+ * in one call (the serving-loop form of the path; the paper has no
+ * counterpart: its path starts and ends in device memory). On `stream`, all
+ * asynchronous: copy x_host (bf16 [T][H]) into x_dev and logits_host
+ * (f32 [T][E]) into logits_dev, then moe_route, moe_dispatch,
+ * moe_expert_synthetic and moe_combine into out_dev (bf16 [T][H]), then copy
+ * out_dev into out_host. bufs: the device buffers of one batch (as for
+ * dbo_step, sized for T tokens); s: device f32[E]. Host buffers should be
+ * page-locked, or the copies do not overlap other streams' work. The call
+ * returns before the work completes: synchronise `stream` before reading
+ * out_host or reusing x_host, logits_host or the device buffers. Two streams
+ * with two buffer sets, used alternately, overlap one batch's copies with
+ * the neighbouring batch's kernels. Errors as the four calls return them. */
+int moe_path_host(const moe_problem *p, const void *x_host, const float *logits_host,
+                  const float *s, void *x_dev, float *logits_dev,
+                  const moe_ubatch_bufs *bufs, void *out_dev, void *out_host, void *stream);
+
 /* Event timing of the overlapped pair of the last dbo_step that recorded it
  * (milliseconds, from CUDA events). overlap_fraction = time both kernels were
  * running / the shorter kernel's duration, in [0, 1]. */

@@ -395,6 +395,40 @@ def test_dbo_layers_full_size_as_benchmarked():
     ctx.close()
 
 
+@pytest.mark.parametrize("name", ["tiny", "dsv3_fp8"])
+def test_path_host_equals_the_device_path(name):
+    """moe_path_host (host x and logits in, host out, one call per batch),
+    alternated over two streams and buffer sets as a serving loop would:
+    every batch's host output equals the device-resident path's output."""
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev
+    w = W.WORKLOADS[name]
+    x, lg, s = W.make_x(w), W.make_logits(w), W.expert_scale(w)
+    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
+    b = M.alloc_buffers(p, "cuda:0")
+    sd = to_dev(s)
+    ref = torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0")
+    M.run_path(p, to_dev(x), to_dev(lg), sd, b, ref)
+    torch.cuda.synchronize()
+    ref_h = ref.cpu()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    paths, outs = [], []
+    for j in range(2):
+        xp = torch.from_numpy(x.view(np.int16)).pin_memory()
+        lp = torch.from_numpy(lg).pin_memory()
+        op = torch.full((w.T, w.H), 7, dtype=torch.int16).pin_memory()
+        outs.append(op)
+        paths.append(M.HostPath(p, xp, lp, sd, torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0"),
+                                torch.empty((w.T, w.E), dtype=torch.float32, device="cuda:0"),
+                                M.alloc_buffers(p, "cuda:0"), torch.empty_like(ref), op, streams[j]))
+    for i in range(4):
+        paths[i % 2]()
+    torch.cuda.synchronize()
+    for op in outs:
+        assert torch.equal(op, ref_h)
+
+
 def test_layer_stand_in_is_exact():
     import torch
     import combine_router_top_gb300 as M
