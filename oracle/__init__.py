@@ -45,6 +45,8 @@ def lib():
             "oracle_scale_rows": [i64, P, C.c_float, P],
             "oracle_gemm_fp8_row": [i32, i32, P, P, P, P, P],
             "oracle_expert_gemm_fp8": [i32, i32, i32, i32, P, P, P, P, P, P],
+            "oracle_gemm_bf16_row": [i32, i32, P, P, P],
+            "oracle_expert_gemm_bf16": [i32, i32, i32, i32, P, P, P, P],
         }.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -189,6 +191,28 @@ def gemm_fp8_row(q_row, a_scale_row, w_q_e, w_scale_e):
                                      _p(np.ascontiguousarray(w_q_e, dtype=np.uint8)),
                                      _p(np.ascontiguousarray(w_scale_e, dtype=np.float32)), _p(y)),
            "oracle_gemm_fp8_row")
+    return y
+
+
+def expert_gemm_bf16(recv_x, counts, w):
+    """Grouped bf16 GEMM on the dispatch layout: y[e][r] = bf16(sum_i x[e][r][i] * w[e][n][i]) (double sums)
+    for r < min(counts[e], C); other rows zero. recv_x [E][C][K], w [E][N][K] bf16 bits -> y [E][C][N]."""
+    E, Cap, K = recv_x.shape
+    N = w.shape[1]
+    y = np.zeros((E, Cap, N), dtype=np.uint16)
+    _check(lib().oracle_expert_gemm_bf16(K, N, E, Cap, _p(np.ascontiguousarray(recv_x, dtype=np.uint16)),
+                                         _p(np.ascontiguousarray(counts, dtype=np.int32)),
+                                         _p(np.ascontiguousarray(w, dtype=np.uint16)), _p(y)),
+           "oracle_expert_gemm_bf16")
+    return y
+
+
+def gemm_bf16_row(x_row, w_e):
+    """One output row of the bf16 grouped GEMM: x_row [K], w_e [N][K] bf16 bits -> [N] bf16 bits."""
+    N, K = w_e.shape
+    y = np.empty(N, dtype=np.uint16)
+    _check(lib().oracle_gemm_bf16_row(K, N, _p(np.ascontiguousarray(x_row, dtype=np.uint16)),
+                                      _p(np.ascontiguousarray(w_e, dtype=np.uint16)), _p(y)), "oracle_gemm_bf16_row")
     return y
 
 

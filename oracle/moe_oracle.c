@@ -29,7 +29,8 @@
  *   - The grouped GEMM that stands in for the experts maps each dispatched
  *     fp8 row through one random e4m3 weight matrix per expert (128 x 128
  *     weight blocks with an fp32 scale each), exactly, then rounds once to
- *     bf16 (nearest-even).
+ *     bf16 (nearest-even); each dispatched bf16 row through one random bf16
+ *     weight matrix per expert, in double, then once to bf16.
  *
  * Layouts (row-major):
  *   logits[T][E] f32; topk_idx[T][k] i32; topk_w[T][k] f32; slot[T][k] i32;
@@ -456,6 +457,48 @@ int oracle_expert_gemm_fp8(int32_t K, int32_t N, int32_t E, int32_t C, const uin
         for (int32_t r = 0; r < rows; ++r) {
             const int64_t row = (int64_t)e * C + r;
             if (oracle_gemm_fp8_row(K, N, recv_q + row * K, recv_scale + row * kb, we, se, y + row * N) != 0)
+                return -1;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Grouped expert GEMM on the bf16 dispatch layout (the same stand-in for the */
+/* experts, for bf16 rows; random bf16 weights, one map of N outputs each):   */
+/*   y[e][r][n] = bf16( sum_i x[e][r][i] * w[e][n][i] )                       */
+/* The products and the sum are taken in double (a bf16 product has at most  */
+/* 16 significant bits; the sum rounds only far below bf16 precision) and    */
+/* the result is rounded once to bf16, to nearest, ties to even; an exact    */
+/* zero comes out as +0.                                                     */
+/* ------------------------------------------------------------------------ */
+int oracle_gemm_bf16_row(int32_t K, int32_t N, const uint16_t *x_row, const uint16_t *w, uint16_t *y_row)
+{
+    if (K < 1 || N < 1)
+        return -1;
+    for (int32_t n = 0; n < N; ++n) {
+        const uint16_t *wn = w + (int64_t)n * K;
+        double acc = 0.0;
+        for (int32_t i = 0; i < K; ++i)
+            acc += (double)bf16_decode(x_row[i]) * (double)bf16_decode(wn[i]);
+        y_row[n] = bf16_encode_rne_double(acc);
+    }
+    return 0;
+}
+
+/* Every expert, rows r < min(counts[e], C); other rows untouched.
+ * recv_x[E][C][K] bf16, w[E][N][K] bf16, y[E][C][N] bf16. */
+int oracle_expert_gemm_bf16(int32_t K, int32_t N, int32_t E, int32_t C, const uint16_t *recv_x,
+                            const int32_t *counts, const uint16_t *w, uint16_t *y)
+{
+    if (E < 1 || C < 1 || K < 1 || N < 1)
+        return -1;
+    for (int32_t e = 0; e < E; ++e) {
+        const int32_t kept_rows = counts[e] < C ? counts[e] : C;
+        const uint16_t *we = w + (int64_t)e * N * K;
+        for (int32_t r = 0; r < kept_rows; ++r) {
+            const int64_t row = (int64_t)e * C + r;
+            if (oracle_gemm_bf16_row(K, N, recv_x + row * K, we, y + row * N) != 0)
                 return -1;
         }
     }

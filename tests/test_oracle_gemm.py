@@ -160,3 +160,68 @@ def test_weight_generator_draws_the_stated_distribution():
     assert ws.min() >= 2.0 ** -8 and ws.max() < 2.0 ** -7
     a, b = W.make_weights(w_, e0=5, ne=2)
     assert np.array_equal(a, wq[5:7]) and np.array_equal(b, ws[5:7])
+
+
+# ---- bf16 rows, bf16 weights --------------------------------------------------
+
+def random_bf16(rng, shape, scale=1.0):
+    return torch.from_numpy((rng.standard_normal(shape) * scale).astype(np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("K,N", [(256, 384), (72, 40), (1, 3)])
+def test_bf16_gemm_equals_float64_matmul(K, N):
+    rng = np.random.default_rng(K * 7 + N)
+    E, C = 3, 4
+    x = random_bf16(rng, (E, C, K))
+    w = random_bf16(rng, (E, N, K), 2.0 ** -5)
+    counts = np.array([4, 1, 0], dtype=np.int32)
+    y = O.expert_gemm_bf16(x, counts, w)
+    ref = np.einsum("eck,enk->ecn", bf16_values(x), bf16_values(w))
+    for e in range(E):
+        r = min(int(counts[e]), C)
+        assert_nearest_bf16(y[e, :r], ref[e, :r])
+        assert not y[e, r:].any()
+
+
+def test_bf16_identity_and_permutation_weights_are_exact():
+    """W = I gives the rows back (zeros as +0); a permutation that is not an
+    involution, with power-of-two weights 2^(n mod 5), gives x[pi(n)] * 2^(n mod 5):
+    a transposed W fails."""
+    rng = np.random.default_rng(11)
+    K = 96
+    x = random_bf16(rng, (1, 3, K))
+    eye = np.zeros((1, K, K), dtype=np.uint16)
+    eye[0, np.arange(K), np.arange(K)] = 0x3F80
+    y = O.expert_gemm_bf16(x, np.array([3], dtype=np.int32), eye)
+    assert np.array_equal(y, bf16_bits_exact(bf16_values(x) + 0.0))
+    pi = rng.permutation(K)
+    assert not np.array_equal(pi[pi], np.arange(K))
+    n = np.arange(K)
+    wp = np.zeros((1, K, K), dtype=np.uint16)
+    wp[0, n, pi] = bf16_bits_exact((2.0 ** (n % 5)).astype(np.float64))
+    y = O.expert_gemm_bf16(x, np.array([3], dtype=np.int32), wp)
+    want = bf16_values(x[0][:, pi]) * (2.0 ** (n % 5))[None, :] + 0.0
+    assert np.array_equal(y[0], bf16_bits_exact(want))
+
+
+def test_bf16_rounding_is_once_to_nearest_even():
+    """1 + 2^-8 ties to 1.0; 1 + 2^-8 + 2^-40 must round up to 1 + 2^-7."""
+    x = np.zeros((1, 2, 3), dtype=np.uint16)
+    x[0, 0, :2] = [0x3F80, 0x3B80]            # 1, 2^-8
+    x[0, 1, :] = [0x3F80, 0x3B80, 0x2B80]     # 1, 2^-8, 2^-40
+    w = np.full((1, 1, 3), 0x3F80, dtype=np.uint16)
+    y = O.expert_gemm_bf16(x, np.array([2], dtype=np.int32), w)
+    assert [hex(v) for v in y[0, :, 0]] == ["0x3f80", "0x3f81"]
+
+
+def test_bf16_weight_generator_and_row_entry():
+    w_ = W.WORKLOADS["tiny"]
+    wb = W.make_weights_bf16(w_)
+    v = bf16_values(wb)
+    assert wb.shape == (8, 256, 256) and abs(v.std() - 2.0 ** -5) < 2.0 ** -9 and abs(v.mean()) < 2.0 ** -10
+    assert np.array_equal(W.make_weights_bf16(w_, e0=3, ne=2), wb[3:5])
+    rng = np.random.default_rng(3)
+    x = random_bf16(rng, (8, 4, 256))
+    y = O.expert_gemm_bf16(x, np.full(8, 4, dtype=np.int32), wb)
+    assert np.array_equal(O.gemm_bf16_row(x[5, 2], wb[5]), y[5, 2])

@@ -69,6 +69,14 @@ MUTANTS = {
     "gemm_double_rounding": ("y_row[n] = bf16_encode_rne_double(acc);", "y_row[n] = bf16_encode_rne((float)acc);"),
     # gemm: rows past the count computed too
     "gemm_rows_unclipped": ("const int32_t rows = counts[e] < C ? counts[e] : C;", "const int32_t rows = C;"),
+    # bf16 gemm: the weight read transposed, kept in bounds
+    "gemm_bf16_weight_transposed": ("acc += (double)bf16_decode(x_row[i]) * (double)bf16_decode(wn[i]);",
+                                    "acc += (double)bf16_decode(x_row[i]) * (double)bf16_decode(w[(int64_t)(i % N) * K + n % K]);"),
+    # bf16 gemm: accumulation in float
+    "gemm_bf16_float_sum": ("        double acc = 0.0;\n        for (int32_t i = 0; i < K; ++i)\n            acc +=",
+                            "        float acc = 0.0f;\n        for (int32_t i = 0; i < K; ++i)\n            acc +="),
+    # bf16 gemm: rows past the count computed too
+    "gemm_bf16_rows_unclipped": ("const int32_t kept_rows = counts[e] < C ? counts[e] : C;", "const int32_t kept_rows = C;"),
     # layer stand-in: the scale factor ignored
     "scale_rows_ignores_a": ("out[i] = bf16_encode_rne(bf16_decode(in[i]) * a);", "out[i] = bf16_encode_rne(bf16_decode(in[i]));"),
 }

@@ -32,6 +32,8 @@ fp32 scale per 128 x 128 block, 2^-8 * (1 + u) with u uniform in [0, 1).
 make_weights draws them with SplitMix64 (small cases, checked by the oracle);
 make_weights_device draws the same distribution with PyTorch's seeded device
 generator (full-size runs, where a host draw of gigabytes would take minutes).
+bf16 weights (for bf16 rows): bf16(float32(N(0,1) * 2^-5)), host (make_weights_bf16)
+or device (make_weights_bf16_device, PyTorch's generator).
 """
 from __future__ import annotations
 
@@ -49,6 +51,7 @@ STREAM_X = 1
 STREAM_LOGITS = 2
 STREAM_W = 3
 STREAM_W_SCALE = 4
+STREAM_W_BF16 = 5
 W_MAG_LO, W_MAG_N = 0x30, 72          # magnitude codes 0x30..0x77
 
 DTYPE_BF16 = 0
@@ -191,3 +194,27 @@ def make_weights_device(w: Workload, device, N: int | None = None):
     u = torch.rand((w.E, N // 128, w.H // 128), generator=g, device=device, dtype=torch.float64)
     w_scale = ((1.0 + u) * 2.0 ** -8).to(torch.float32)
     return w_q, w_scale
+
+
+def make_weights_bf16(w: Workload, e0: int = 0, ne: int | None = None, N: int | None = None) -> np.ndarray:
+    """bf16 weights of the grouped GEMM for bf16 rows, experts e0..e0+ne-1:
+    w[ne][N][H] bit patterns of bf16(float32(N(0,1) * 2^-5))."""
+    ne = w.E - e0 if ne is None else ne
+    N = w.H if N is None else N
+    per = N * w.H
+    v = (normals(w.seed, STREAM_W_BF16, e0 * per, ne * per) * 2.0 ** -5).astype(np.float32)
+    return _to_bf16_bits(v).reshape(ne, N, w.H)
+
+
+def make_weights_bf16_device(w: Workload, device, N: int | None = None):
+    """All experts' bf16 weights drawn on `device` by PyTorch's seeded generator
+    (same distribution as make_weights_bf16, not the same values), as int16 bits."""
+    import torch
+    N = w.H if N is None else N
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed * 65536 + STREAM_W_BF16)
+    out = torch.empty((w.E, N, w.H), dtype=torch.int16, device=device)
+    for e in range(w.E):
+        out[e] = (torch.randn((N, w.H), generator=g, device=device, dtype=torch.float32) * 2.0 ** -5).to(
+            torch.bfloat16).view(torch.int16)
+    return out
