@@ -80,6 +80,7 @@ def lib() -> C.CDLL:
             "moe_route_dispatch": ([pp, P, P, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
             "moe_expert_synthetic": ([pp, P, P, P, P, P, P], i),
             "moe_expert_gemm_fp8": ([pp, P, P, P, P, P, P, P], i),
+            "moe_expert_gemm_bf16": ([pp, P, P, P, P, P], i),
             "moe_ready_flags_bytes": ([pp], C.c_size_t),
             "moe_path_host": ([pp, P, P, P, P, P, C.POINTER(moe_ubatch_bufs), P, P, P], i),
             "moe_expert_combine": ([pp, P, P, P, P, P, P, P, P, P, P, C.c_size_t, C.c_uint32, P], i),
@@ -102,7 +103,7 @@ def lib() -> C.CDLL:
 
 EXPORTS = ("moe_status_string", "moe_validate", "moe_device_status", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
            "moe_dispatch", "moe_route_dispatch_workspace_bytes", "moe_route_dispatch",
-           "moe_expert_synthetic", "moe_expert_gemm_fp8", "moe_ready_flags_bytes", "moe_expert_combine", "moe_path_host",
+           "moe_expert_synthetic", "moe_expert_gemm_fp8", "moe_expert_gemm_bf16", "moe_ready_flags_bytes", "moe_expert_combine", "moe_path_host",
            "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
            "moe_layer_stand_in", "dbo_layers", "dbo_layers_capture", "dbo_graph_launch")
 
@@ -198,6 +199,12 @@ def moe_expert_gemm_fp8(p, recv_q, recv_scale, counts, w_q, w_scale, y, stream=N
     rc = lib().moe_expert_gemm_fp8(C.byref(p), _ptr(recv_q), _ptr(recv_scale), _ptr(counts), _ptr(w_q),
                                    _ptr(w_scale), _ptr(y), _stream(stream))
     _check("moe_expert_gemm_fp8", rc)
+
+
+def moe_expert_gemm_bf16(p, recv_x, counts, w, y, stream=None):
+    """Grouped bf16 GEMM on the dispatch layout (tensor cores): y[e][r] = bf16(row . W_e^T) on kept rows."""
+    rc = lib().moe_expert_gemm_bf16(C.byref(p), _ptr(recv_x), _ptr(counts), _ptr(w), _ptr(y), _stream(stream))
+    _check("moe_expert_gemm_bf16", rc)
 
 
 def moe_ready_flags_bytes(p: moe_problem) -> int:

@@ -43,13 +43,13 @@ namespace {
 
 constexpr int kBM = 128;                         // rows of one expert per tile
 constexpr int kBN = 256;                         // outputs per tile (128 or 256)
-constexpr int kBK = 128;                         // inputs per block (one scale per row and block)
+constexpr int kBK = 128;                         // bytes of input per row and block: 128 e4m3 (one scale) or 64 bf16
 constexpr int kNumAcc = 512 / kBN;               // fp32 accumulators that fill the 512 TMEM columns
 constexpr int kGemmStages = (196 * 1024) / (kBM * kBK + kBN * kBK);
 constexpr int kGemmEpiWarps = 16;
 constexpr int kGemmThreads = 32 * (2 + kGemmEpiWarps + 2);   // + 2 idle warps: 20 warps, 96 registers each
-constexpr uint32_t kATileBytes = kBM * kBK;      // e4m3: 16 KB
-constexpr uint32_t kBTileBytes = kBN * kBK;      // e4m3: 32 KB
+constexpr uint32_t kATileBytes = kBM * kBK;      // 16 KB
+constexpr uint32_t kBTileBytes = kBN * kBK;      // 32 KB
 constexpr uint32_t kGemmStageBytes = kATileBytes + kBTileBytes;
 constexpr uint32_t kGemmTmemCols = kNumAcc * kBN;   // all 512 columns
 constexpr int kEpiCols = kBN / 4;                // columns per promotion warp (4 per TMEM lane quadrant)
@@ -66,12 +66,14 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor: kind::f8f6f4, A and B e4m3, both K-major, fp32
-// accumulator, M = 128, N = 256.
-constexpr uint32_t kIdescF8 = (1u << 4)                          // D format f32
-                              | (0u << 7) | (0u << 10)           // A, B e4m3
-                              | ((uint32_t)(kBN >> 3) << 17)     // N / 8
-                              | ((uint32_t)(kBM >> 4) << 24);    // M / 16
+// Instruction descriptors, both operands K-major, fp32 accumulator, M = 128,
+// N = kBN: kind::f8f6f4 with A and B e4m3 (format 0), kind::f16 with A and B
+// bf16 (format 1).
+constexpr uint32_t kIdescShape = (1u << 4)                          // D format f32
+                                 | ((uint32_t)(kBN >> 3) << 17)     // N / 8
+                                 | ((uint32_t)(kBM >> 4) << 24);    // M / 16
+constexpr uint32_t kIdescF8 = kIdescShape | (0u << 7) | (0u << 10);
+constexpr uint32_t kIdescBF16 = kIdescShape | (1u << 7) | (1u << 10);
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -84,12 +86,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-__device__ __forceinline__ void mma_f8(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(kIdescF8), "r"(accumulate)
-        : "memory");
+// One MMA of 32 bytes of K per row: 32 e4m3 (kind::f8f6f4) or 16 bf16 (kind::f16).
+template <bool FP8>
+__device__ __forceinline__ void mma_k32b(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
+    if constexpr (FP8)
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
+            "l"(a), "l"(b), "r"(kIdescF8), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem_d),
+            "l"(a), "l"(b), "r"(kIdescBF16), "r"(accumulate)
+            : "memory");
 }
 
 // Arrives once on the mbarrier when every MMA this thread issued so far is complete.
@@ -142,8 +153,12 @@ struct TileList {
     }
 };
 
+// FP8: per-block promotion (fresh accumulator per block of 128 inputs, scaled
+// in registers). BF16: no scales, so one accumulator holds a whole tile and
+// the promotion warps only convert and store it.
+template <bool FP8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                        const float *__restrict__ a_scale, const int32_t *__restrict__ counts,
                        const float *__restrict__ w_scale, uint16_t *__restrict__ y, int H, int C, int E,
                        unsigned *status) {
@@ -156,7 +171,8 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
     __shared__ int s_kept[kMaxExperts];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nkb = H / kBK, nb = H / 128;
+    const int nkb = FP8 ? H / kBK : H / (kBK / 2), nb = H / 128;
+    const int kb_elems = FP8 ? kBK : kBK / 2;           // inputs per block (TMA x coordinate step)
     const int n_tiles = (H + kBN - 1) / kBN;
     const uint32_t smem0 = (smem_u32(gemm_smem_raw) + 1023u) & ~1023u;
 
@@ -213,7 +229,7 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
     const uint32_t tmem = s_tmem;
 
     uint32_t issued = 0;                          // producer: stages loaded
-    uint32_t committed = 0;                       // MMA issuer: blocks committed
+    uint32_t committed = 0;                       // MMA issuer: accumulators committed
     if (warp == 0) {
         if (lane == 0) {
             uint32_t g = 0;
@@ -229,31 +245,39 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
                         break;
                     const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kATileBytes;
                     mbar_expect_tx(&full_bar[s], kGemmStageBytes);
-                    tma_load_2d(sa, &map_a, smem_u32(&full_bar[s]), kb * kBK, row_a);
-                    tma_load_2d(sb, &map_b, smem_u32(&full_bar[s]), kb * kBK, row_b);
+                    tma_load_2d(sa, &map_a, smem_u32(&full_bar[s]), kb * kb_elems, row_a);
+                    tma_load_2d(sb, &map_b, smem_u32(&full_bar[s]), kb * kb_elems, row_b);
                     issued = g + 1;
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            uint32_t g = 0;
-            for (int t = blockIdx.x; t < total && !s_abort; t += gridDim.x) {
+            uint32_t g = 0;                       // blocks consumed (stage ring)
+            uint32_t a = 0;                       // accumulators used (FP8: per block, BF16: per tile)
+            bool stop = false;
+            for (int t = blockIdx.x; t < total && !stop && !s_abort; t += gridDim.x) {
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
-                    const int s = g % kGemmStages, buf = g % kNumAcc;
-                    if (!gemm_wait(smem_u32(&full_bar[s]), (g / kGemmStages) & 1, &s_abort)) break;
-                    if (g >= kNumAcc &&
-                        !gemm_wait(smem_u32(&tempty_bar[buf]), ((g / kNumAcc) + 1) & 1, &s_abort))
+                    const int s = g % kGemmStages;
+                    const int buf = a % kNumAcc;
+                    if (!gemm_wait(smem_u32(&full_bar[s]), (g / kGemmStages) & 1, &s_abort)) { stop = true; break; }
+                    if ((FP8 || kb == 0) && a >= kNumAcc &&
+                        !gemm_wait(smem_u32(&tempty_bar[buf]), ((a / kNumAcc) + 1) & 1, &s_abort)) {
+                        stop = true;
                         break;
+                    }
                     tc_fence_after();
                     const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kATileBytes;
                     const uint32_t d = tmem + buf * kBN;
 #pragma unroll
                     for (int k = 0; k < kBK / 32; ++k)
-                        mma_f8(d, umma_desc_sw128(sa + 32 * k), umma_desc_sw128(sb + 32 * k), k > 0 ? 1u : 0u);
+                        mma_k32b<FP8>(d, umma_desc_sw128(sa + 32 * k), umma_desc_sw128(sb + 32 * k),
+                                      (k > 0 || (!FP8 && kb > 0)) ? 1u : 0u);
                     mma_commit(smem_u32(&empty_bar[s]));
-                    mma_commit(smem_u32(&tfull_bar[buf]));
-                    committed = g + 1;
+                    if (FP8 || kb == nkb - 1) {
+                        mma_commit(smem_u32(&tfull_bar[buf]));
+                        committed = ++a;
+                    }
                 }
             }
         }
@@ -266,9 +290,43 @@ expert_gemm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_c
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             int e, nt, mt, rows;
             tiles.decode(t, e, nt, mt, rows);
-            const int nblk = (nt * kBN + cg * kEpiCols) / 128;   // 128-output block of this warp's columns
-            const bool live = r < rows && nblk < nb;
+            const int col0 = nt * kBN + cg * kEpiCols;         // this warp's first output column
+            const int nblk = col0 / 128;                       // its 128-output weight-scale block
+            const bool live = r < rows && col0 < H;
             const size_t grow = (size_t)e * C + (size_t)mt * kBM + r;
+            if constexpr (!FP8) {
+                // the tile's whole sum is in one accumulator: convert and store
+                const int buf = g % kNumAcc;
+                int got = 0;
+                if (lane == 0) got = gemm_wait(smem_u32(&tfull_bar[buf]), (g / kNumAcc) & 1, &s_abort) ? 1 : 0;
+                if (!__shfl_sync(kFull, got, 0)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + buf * kBN + cg * kEpiCols;
+                uint4 *dst = reinterpret_cast<uint4 *>(y + grow * H + (size_t)nt * kBN + cg * kEpiCols);
+#pragma unroll
+                for (int c = 0; c < kEpiCols / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + 16 * c, v);
+                    tmem_ld_wait();
+                    if (live) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            dst[2 * c + h] = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[8 * h + 0]), __uint_as_float(v[8 * h + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * h + 2]), __uint_as_float(v[8 * h + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * h + 4]), __uint_as_float(v[8 * h + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * h + 6]), __uint_as_float(v[8 * h + 7])));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                ++g;
+                continue;
+            }
             const float *sa_row = a_scale + grow * nb;
             const float *sw_row = w_scale + ((size_t)e * nb + (live ? nblk : 0)) * nb;
             float acc[kEpiCols];
@@ -349,18 +407,48 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// A [rows][cols] byte matrix read in tiles of box_rows x 128 bytes, 128-byte
-// swizzled; rows past the end read as zero.
-bool encode_tile_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// A [rows][cols] matrix of 1- or 2-byte elements read in tiles of box_rows x
+// 128 bytes, 128-byte swizzled; rows past the end read as zero.
+bool encode_tile_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                     int elem_bytes) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint64_t strides[1] = {cols * (cuuint64_t)elem_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(kBK / elem_bytes), box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool FP8>
+int launch_gemm(const Dims &d, const void *recv, const float *recv_scale, const int32_t *counts, const void *w,
+                const float *w_scale, void *y, void *stream) {
+    const int eb = FP8 ? 1 : 2;
+    CUtensorMap map_a, map_b;
+    if (!encode_tile_map(&map_a, recv, (uint64_t)d.E * d.C, (uint64_t)d.H, kBM, eb) ||
+        !encode_tile_map(&map_b, w, (uint64_t)d.E * d.H, (uint64_t)d.H, kBN, eb))
+        return MOE_ERR_CUDA;
+    unsigned *status = device_status_word();
+    if (status == nullptr) return MOE_ERR_CUDA;
+    static bool smem_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (!smem_set[dev]) {
+        if (cudaFuncSetAttribute(expert_gemm_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kGemmSmemBytes) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        smem_set[dev] = true;
+    }
+    int grid = sm_count();                        // persistent: one CTA per SM
+    if (d.max_blocks > 0 && d.max_blocks < grid) grid = d.max_blocks;
+    if (launch_pdl_smem(expert_gemm_kernel<FP8>, grid, kGemmThreads, kGemmSmemBytes, as_stream(stream), map_a,
+                        map_b, recv_scale, counts, w_scale, static_cast<uint16_t *>(y), d.H, d.C, d.E, status) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 }  // namespace
@@ -378,26 +466,18 @@ extern "C" int moe_expert_gemm_fp8(const moe_problem *p, const void *recv_q, con
     if (!aligned(recv_q, 16) || !aligned(w_q, 16) || !aligned(y, 16) || !aligned(recv_scale, 4) ||
         !aligned(w_scale, 4) || !aligned(counts, 4))
         return MOE_ERR_INVALID_ARG;
-    CUtensorMap map_a, map_b;
-    if (!encode_tile_map(&map_a, recv_q, (uint64_t)d.E * d.C, (uint64_t)d.H, kBM) ||
-        !encode_tile_map(&map_b, w_q, (uint64_t)d.E * d.H, (uint64_t)d.H, kBN))
-        return MOE_ERR_CUDA;
-    unsigned *status = device_status_word();
-    if (status == nullptr) return MOE_ERR_CUDA;
-    static bool smem_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    if (!smem_set[dev]) {
-        if (cudaFuncSetAttribute(expert_gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kGemmSmemBytes) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        smem_set[dev] = true;
-    }
-    int grid = sm_count();                        // persistent: one CTA per SM
-    if (d.max_blocks > 0 && d.max_blocks < grid) grid = d.max_blocks;
-    if (launch_pdl_smem(expert_gemm_fp8_kernel, grid, kGemmThreads, kGemmSmemBytes, as_stream(stream), map_a, map_b,
-                        recv_scale, counts, w_scale, static_cast<uint16_t *>(y), d.H, d.C, d.E, status) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
-    return MOE_OK;
+    return launch_gemm<true>(d, recv_q, recv_scale, counts, w_q, w_scale, y, stream);
+}
+
+extern "C" int moe_expert_gemm_bf16(const moe_problem *p, const void *recv_x, const int32_t *counts,
+                                    const void *w, void *y, void *stream) {
+    using namespace moe;
+    Dims d;
+    int rc = check_problem(p, &d);
+    if (rc != MOE_OK) return rc;
+    if (d.dtype != MOE_DTYPE_BF16 || d.H % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!recv_x || !counts || !w || !y) return MOE_ERR_INVALID_ARG;
+    if (!aligned(recv_x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(counts, 4))
+        return MOE_ERR_INVALID_ARG;
+    return launch_gemm<false>(d, recv_x, nullptr, counts, w, nullptr, y, stream);
 }

@@ -215,11 +215,25 @@ int moe_expert_synthetic(const moe_problem *p, const void *recv, const float *re
  * (row n holds the H inputs of output n); w_scale f32[E][H/128][H/128]; y bf16
  * [E][C][H]; counts i32[E] as moe_route writes them. recv_q, w_q and y 16-byte
  * aligned. Requires dispatch_dtype == MOE_DTYPE_FP8_E4M3_B128 (else
- * MOE_ERR_UNSUPPORTED); max_blocks is ignored (one CTA per 128 x 128 output
- * tile). Launched as a programmatic dependent of the previous kernel. */
+ * MOE_ERR_UNSUPPORTED); max_blocks caps the persistent grid (one CTA per SM
+ * by default). Launched as a programmatic dependent of the previous kernel. */
 int moe_expert_gemm_fp8(const moe_problem *p, const void *recv_q, const float *recv_scale,
                         const int32_t *counts, const void *w_q, const float *w_scale,
                         void *y, void *stream);
+
+/* Grouped expert GEMM on the bf16 dispatch layout, on the tensor cores: the
+ * same expert stand-in for bf16 rows, one H -> H linear map per expert with
+ * random bf16 weights (no activation):
+ *   y[e][r][n] = bf16( sum_i recv_x[e][r][i] * w[e][n][i] )
+ * for r < min(counts[e], C); other rows of y are not written. The products
+ * are exact and summed on the tensor cores in fp32 (tcgen05.mma kind::f16),
+ * then rounded to bf16 (nearest even). recv_x bf16 [E][C][H] as moe_dispatch
+ * writes it; w bf16 [E][H][H], output index major; y bf16 [E][C][H]; all
+ * 16-byte aligned. Requires dispatch_dtype == MOE_DTYPE_BF16 and H % 64 == 0
+ * (else MOE_ERR_UNSUPPORTED); max_blocks caps the persistent grid. Launched as
+ * a programmatic dependent of the previous kernel. */
+int moe_expert_gemm_bf16(const moe_problem *p, const void *recv_x, const int32_t *counts,
+                         const void *w, void *y, void *stream);
 
 /* Synthetic expert and combine in one kernel, readiness tracked per expert
  * row instead of per kernel: [PMC §Further Improvements] notes that buffers

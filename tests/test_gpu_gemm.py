@@ -165,3 +165,113 @@ def test_gemm_full_size_sampled_rows(name):
         ref = O.gemm_fp8_row(rq[e, r], rs[e, r], wq_e, ws_e)
         worst = max(worst, check_row(yh[e, r], ref, abs_bound_row(rq[e, r], rs[e, r], wq_e, ws_e)))
     print(f"{name} sampled rows: max |err| / S = {worst:.3g}")
+
+
+# ---- bf16 rows, bf16 weights (tcgen05 kind::f16) --------------------------------
+#
+# Tolerance: bf16 x bf16 products are exact in fp32 and the tensor cores sum
+# them in fp32; the worst case of a sequential fp32 sum of K <= 8192 terms is
+# K * 2^-24 * S <= 2^-11 * S with S = sum_i |x_i * w_i|. Bar:
+#     |y_gpu - y_oracle| <= 2^-11 * S + 1 bf16 ulp of y_oracle.
+
+def bf16_abs(bits):
+    return np.abs(bf16_f64(bits))
+
+
+def check_row_bf16(y_gpu, y_ref, x_row, w_e):
+    S = bf16_abs(w_e) @ bf16_abs(x_row)
+    g, r = bf16_f64(y_gpu), bf16_f64(y_ref)
+    assert np.all(np.isfinite(g)), "non-finite output"
+    a = np.abs(r)
+    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 7), 2.0 ** -133)
+    err = np.abs(g - r)
+    assert np.all(err <= 2.0 ** -11 * S + ulp), f"max err/S {np.max(err / np.maximum(S, 1e-300)):.3g}"
+    return float(np.max(err / np.maximum(S, 1e-300)))
+
+
+def oracle_dispatch_bf16(w: W.Workload):
+    x, lg = W.make_x(w), W.make_logits(w)
+    idx, _ = O.route(lg, w.k)
+    c = O.count(idx, w.E, w.R, w.C)
+    rx, _ = O.dispatch_bf16(x, idx, c["slot"], w.E, w.C)
+    return rx, c["counts"]
+
+
+CASES_BF16 = {
+    # one block of 64 inputs; 64 valid outputs of a 256-output tile
+    "H64": (W.Workload("b64", T=40, H=64, E=3, k=2, R=1, C=32, seed=301), None),
+    # 192 of 256 outputs valid in the only output tile; 3 blocks
+    "H192": (W.Workload("b192", T=60, H=192, E=4, k=2, R=2, C=40, seed=302), None),
+    # two row tiles per expert, the stage ring wrapping
+    "H512_two_row_tiles": (W.Workload("b512", T=150, H=512, E=2, k=2, R=1, C=160, seed=303), None),
+    "H2048": (W.Workload("b2048", T=24, H=2048, E=2, k=2, R=2, C=32, seed=304), None),
+    "overflow_and_empty": (W.Workload("bov", T=64, H=256, E=8, k=2, R=4, C=8, seed=305), [2, 5]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES_BF16))
+def test_gemm_bf16_matches_oracle(case):
+    import combine_router_top_gb300 as M
+    w, empty = CASES_BF16[case]
+    rx, counts = oracle_dispatch_bf16(w)
+    counts = counts.copy()
+    if empty:
+        counts[empty] = 0
+    wb = W.make_weights_bf16(w)
+    y_ref = O.expert_gemm_bf16(rx, counts, wb)
+    rng = np.random.default_rng(w.seed)
+    rx_dev = rx.copy()
+    for e in range(w.E):                      # rows past the count: garbage bits, NaNs included
+        kept = min(int(counts[e]), w.C)
+        rx_dev[e, kept:] = rng.integers(0, 1 << 16, size=(w.C - kept, w.H), dtype=np.uint16)
+    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, M.MOE_DTYPE_BF16)
+    y = torch.full((w.E, w.C, w.H), SENTINEL, dtype=torch.int32, device=DEV).to(torch.int16)
+    M.moe_expert_gemm_bf16(p, torch.from_numpy(rx_dev.view(np.int16)).to(DEV),
+                           torch.from_numpy(np.ascontiguousarray(counts, dtype=np.int32)).to(DEV),
+                           torch.from_numpy(wb.view(np.int16)).to(DEV), y)
+    torch.cuda.synchronize()
+    assert M.moe_device_status() == M.MOE_OK
+    yh = y.cpu().numpy().view(np.uint16)
+    worst = 0.0
+    for e in range(w.E):
+        kept = min(int(counts[e]), w.C)
+        assert np.all(yh[e, kept:] == SENTINEL), f"expert {e}: rows past the count were written"
+        for r in range(kept):
+            worst = max(worst, check_row_bf16(yh[e, r], y_ref[e, r], rx[e, r], wb[e]))
+    print(f"bf16 {case}: max |err| / S = {worst:.3g}")
+
+
+@pytest.mark.parametrize("name", ["v2lite", "dbo_prefill"])
+def test_gemm_bf16_full_size_sampled_rows(name):
+    """DeepSeek-V2-Lite decode (256 tokens, H 2048, 64 experts) and the 8192-token
+    dual-batch prefill shape (H 7168, 256 experts, C 1024; 26 GB of device-drawn
+    weights): route -> dispatch -> GEMM on the GPU, sampled rows against the
+    oracle fed by its own dispatch."""
+    import combine_router_top_gb300 as M
+    w = W.WORKLOADS["v2lite"] if name == "v2lite" else W.WORKLOADS["dbo"]
+    rx, counts = oracle_dispatch_bf16(w)
+    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, M.MOE_DTYPE_BF16)
+    b = M.alloc_buffers(p, DEV)
+    x = torch.from_numpy(W.make_x(w).view(np.int16)).to(DEV)
+    lg = torch.from_numpy(W.make_logits(w)).to(DEV)
+    M.moe_route(p, lg, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["slot"], b["rank_counts"],
+                b["dropped"], b["workspace"])
+    M.moe_dispatch(p, x, b["topk_idx"], b["slot"], b["recv"], None, b["recv_src"])
+    wb = W.make_weights_bf16_device(w, DEV)
+    y = torch.full((w.E, w.C, w.H), SENTINEL, dtype=torch.int32, device=DEV).to(torch.int16)
+    M.moe_expert_gemm_bf16(p, b["recv"], b["counts"], wb, y)
+    torch.cuda.synchronize()
+    assert M.moe_device_status() == M.MOE_OK
+    assert np.array_equal(b["counts"].cpu().numpy(), counts)
+    kept = np.minimum(counts, w.C)
+    live = [e for e in range(w.E) if kept[e] > 0]
+    emax = int(np.argmax(kept))
+    picks = [(live[0], 0), (live[-1], kept[live[-1]] - 1), (emax, kept[emax] - 1), (emax, min(130, kept[emax] - 1))]
+    worst = 0.0
+    for e, r in picks:
+        yr = y[e, r].cpu().numpy().view(np.uint16)
+        assert np.all(y[e, kept[e]:].cpu().numpy().view(np.uint16) == SENTINEL)
+        w_e = wb[e].cpu().numpy().view(np.uint16)
+        ref = O.gemm_bf16_row(rx[e, r], w_e)
+        worst = max(worst, check_row_bf16(yr, ref, rx[e, r], w_e))
+    print(f"bf16 {name} sampled rows: max |err| / S = {worst:.3g}")
