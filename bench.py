@@ -764,6 +764,60 @@ def run_gemm(args, dev, reps: int = 10, experts: int = 0) -> dict:
         r["device_status"] = M.moe_device_status()
         out[name] = r
         del b, y
+    del wq, ws
+    torch.cuda.empty_cache()
+
+    # bf16 rows, bf16 weights (tcgen05 kind::f16): DeepSeek-V2-Lite decode and
+    # the 8192-token prefill shape (26 GB of weights at H 7168, 256 experts);
+    # the bound is whichever of HBM and the bf16 tensor peak takes longer
+    bf16_burst, bf16_sust = fp8_burst / FP8_PER_BF16, fp8_sust / FP8_PER_BF16
+    cases = [("decode_bf16", W.WORKLOADS["v2lite"]), ("prefill_bf16", W.WORKLOADS["dbo"])]
+    if experts:
+        cases = [(n, w.with_(E=experts, R=min(w.R, experts))) for n, w in cases]
+    for name, w in cases:
+        p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, M.MOE_DTYPE_BF16)
+        b = M.alloc_buffers(p, dev)
+        x = torch.from_numpy(x_of(w).view(np.int16)).to(dev)
+        lg = torch.from_numpy(W.make_logits(w)).to(dev)
+        M.moe_route(p, lg, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["slot"], b["rank_counts"],
+                    b["dropped"], b["workspace"], st)
+        M.moe_dispatch(p, x, b["topk_idx"], b["slot"], b["recv"], None, b["recv_src"], st)
+        wb = W.make_weights_bf16_device(w, dev)
+        y = torch.empty((w.E, w.C, w.H), dtype=torch.int16, device=dev)
+
+        def gemm_bf16():
+            M.moe_expert_gemm_bf16(p, b["recv"], b["counts"], wb, y, st)
+        for _ in range(3):
+            gemm_bf16()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a, z in ev:
+            a.record(st)
+            gemm_bf16()
+            z.record(st)
+        torch.cuda.synchronize()
+        ms = statistics.fmean(a.elapsed_time(z) for a, z in ev)
+        counts = b["counts"].cpu().numpy()
+        kept = int(np.minimum(counts, w.C).sum())
+        active = int((counts > 0).sum())
+        algo_bytes = active * w.H * w.H * 2 + kept * w.H * 2 * 2 + w.E * 4
+        flops = 2.0 * kept * w.H * w.H
+        gbs, tfs = algo_bytes / (ms * 1e-3) / 1e9, flops / (ms * 1e-3) / 1e12
+        hbm_bound = algo_bytes / (hbm * 1e9) >= flops / (bf16_burst * 1e12)
+        r = {"workload": f"{name}: T={w.T}, H={w.H}, E={w.E}, top_k={w.k}, C={w.C}, kept rows {kept}, "
+                         f"{active} experts with rows, bf16 in, bf16 out",
+             "ms": ms, "algorithmic_bytes": algo_bytes, "flops": flops, "GB/s": gbs, "TFLOP/s": tfs, "reps": reps,
+             "roofline": ({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                           "peak_source": f"{hbm_kind} hbm_gbs", "tensor_frac": tfs / bf16_burst, "traffic": None}
+                          if hbm_bound else
+                          {"bound": "tensor", "achieved": tfs, "peak": bf16_burst, "unit": "TFLOP/s",
+                           "frac": tfs / bf16_burst, "frac_of_sustained": tfs / bf16_sust,
+                           "peak_source": f"{fp8_kind.replace(' x 2', '')} bf16 (burst)", "hbm_frac": gbs / hbm,
+                           "traffic": None}),
+             "device_status": M.moe_device_status()}
+        out[name] = r
+        del b, y, wb
+        torch.cuda.empty_cache()
     return out
 
 
