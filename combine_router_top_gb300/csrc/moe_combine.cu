@@ -14,7 +14,8 @@
 //     the routing of a token is held by lanes j < k and broadcast by shuffle.
 //   expert: tasks (kept row, 16-byte piece) are numbered over the kept rows
 //     only, through an exclusive scan of min(counts[e], C) held in shared
-//     memory, so no thread walks empty capacity rows.
+//     memory, so no thread walks empty capacity rows; the fp8 expert writes
+//     its bf16 output through per-warp shared-memory buffers and bulk copies.
 #include <algorithm>
 
 #include "moe_internal.cuh"
@@ -151,24 +152,31 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
 }
 
 // Synthetic expert, fp8 rows: a task is 16 codes (16 bytes in, 32 bytes of
-// bf16 out) with its block scale; a unit is (kept row, 32*U tasks).
+// bf16 out) with its block scale; a unit is (kept row, 32*U tasks). The
+// unit's output (32*U*32 contiguous bytes of one row) is converted into a
+// per-warp shared-memory buffer and written by one bulk copy, so that the
+// 117 MB of output at the DeepSeek-V3 shape leave as bulk copies instead of
+// 16-byte stores (40.6 -> 28.7 us). A warp waits until its previous bulk copy
+// has read the buffer before overwriting it.
 template <int U>
 __global__ void __launch_bounds__(kBlock)
-expert_fp8_kernel(const uint4 *__restrict__ recv_q, const float *__restrict__ recv_scale,
-                  const int32_t *__restrict__ counts, const float *__restrict__ s,
-                  uint4 *__restrict__ y, int E, int C, int H, int segs) {
+expert_fp8_bulk_kernel(const uint4 *__restrict__ recv_q, const float *__restrict__ recv_scale,
+                       const int32_t *__restrict__ counts, const float *__restrict__ s,
+                       uint4 *__restrict__ y, int E, int C, int H, int segs) {
+    extern __shared__ __align__(128) uint4 expert_stage[];   // kWarps x (32 * U * 2) uint4
     __shared__ int32_t off[kMaxExperts + 1];
     __shared__ int32_t warp_tot[32];
     pdl_enter();
     kept_row_offsets(counts, E, C, off, warp_tot);
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint4 *buf = expert_stage + (size_t)warp * (32 * U * 2);
     const unsigned n_tasks = H / 16, nb = H / 128, rows = off[E];
-    for (UnitWalk wk(blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, segs); wk.row < rows;
-         wk.next()) {
+    for (UnitWalk wk(blockIdx.x * kWarps + warp, gridDim.x * kWarps, segs); wk.row < rows; wk.next()) {
         const int e = expert_of_row(off, E, (int)wk.row);
         const size_t row = (size_t)e * C + (wk.row - off[e]);
         const float se = __ldg(s + e);
-        const unsigned t0 = wk.seg * 32 * U + lane;
+        const unsigned first = wk.seg * 32 * U;
+        const unsigned t0 = first + lane;
         uint4 q[U];
         float sc[U];
 #pragma unroll
@@ -178,6 +186,8 @@ expert_fp8_kernel(const uint4 *__restrict__ recv_q, const float *__restrict__ re
                 sc[i] = __ldg(recv_scale + row * nb + ((t0 + 32 * i) >> 3));
             }
         }
+        if (lane == 0) bulk_wait_read_all();             // the previous unit's copy has read the buffer
+        __syncwarp();
 #pragma unroll
         for (int i = 0; i < U; ++i) {
             if (t0 + 32 * i < n_tasks) {
@@ -190,24 +200,41 @@ expert_fp8_kernel(const uint4 *__restrict__ recv_q, const float *__restrict__ re
                     ov[2 * h] = pack_bf16x2(__fmul_rn(__fmul_rn(lo.x, sc[i]), se), __fmul_rn(__fmul_rn(lo.y, sc[i]), se));
                     ov[2 * h + 1] = pack_bf16x2(__fmul_rn(__fmul_rn(hi.x, sc[i]), se), __fmul_rn(__fmul_rn(hi.y, sc[i]), se));
                 }
-                uint4 *o = y + row * (H / 8) + 2 * (t0 + 32 * i);
-                st_v4(o, make_uint4(ov[0], ov[1], ov[2], ov[3]));
-                st_v4(o + 1, make_uint4(ov[4], ov[5], ov[6], ov[7]));
+                buf[2 * (32 * i + lane)] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                buf[2 * (32 * i + lane) + 1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
             }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const unsigned n = min(32u * U, n_tasks - first);
+            bulk_s2g(y + row * (H / 8) + 2 * first, buf, n * 32);
+            bulk_commit();
+        }
     }
+    if (lane == 0) bulk_wait_all();
 }
 
 template <int U>
 int launch_expert_fp8(const Dims &d, long long max_rows, cudaStream_t st, const void *recv, const float *scale,
                       const int32_t *counts, const float *s, void *y) {
-    static int resident = resident_blocks(expert_fp8_kernel<U>, kBlock);
     const int segs = (d.H / 16 + 32 * U - 1) / (32 * U);
     const long long units = max_rows * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+    const size_t smem = (size_t)kWarps * 32 * U * 32;
+    static bool smem_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (!smem_set[dev]) {
+        if (cudaFuncSetAttribute(expert_fp8_bulk_kernel<U>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        smem_set[dev] = true;
+    }
+    static int resident = resident_blocks(expert_fp8_bulk_kernel<U>, kBlock, smem);
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-    if (launch_pdl(expert_fp8_kernel<U>, grid, kBlock, st, static_cast<const uint4 *>(recv), scale, counts, s,
-                   static_cast<uint4 *>(y), d.E, d.C, d.H, segs) != cudaSuccess)
+    if (launch_pdl_smem(expert_fp8_bulk_kernel<U>, grid, kBlock, smem, st, static_cast<const uint4 *>(recv), scale,
+                        counts, s, static_cast<uint4 *>(y), d.E, d.C, d.H, segs) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

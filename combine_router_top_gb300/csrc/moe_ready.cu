@@ -77,6 +77,9 @@ expert_combine_kernel(const uint4 *__restrict__ recv, const float *__restrict__ 
                       unsigned epoch, int T, int H, int E, int k, int C, unsigned *status) {
     __shared__ int32_t off[kMaxExperts + 1];
     __shared__ int32_t warp_tot[32];
+    // fp8: per-warp output buffer of one unit (32 * kSegTasks pieces of 32 bytes)
+    extern __shared__ __align__(128) uint4 ready_stage[];
+    uint4 *stage = ready_stage + (size_t)(threadIdx.x >> 5) * (32 * kSegTasks * 2);
     kept_row_offsets(counts, E, C, off, warp_tot);
     const int lane = threadIdx.x & 31;
     const unsigned gw = blockIdx.x * kRWarps + (threadIdx.x >> 5), G = gridDim.x * kRWarps;
@@ -90,7 +93,8 @@ expert_combine_kernel(const uint4 *__restrict__ recv, const float *__restrict__ 
         const int e = expert_of_row(off, E, (int)wk.row);
         const size_t row = (size_t)e * C + (wk.row - off[e]);
         const float se = __ldg(s + e);
-        const unsigned p0 = wk.seg * 32 * kSegTasks + lane;
+        const unsigned first = wk.seg * 32 * kSegTasks;
+        const unsigned p0 = first + lane;
         uint4 v[kSegTasks];
         float sc[kSegTasks];
 #pragma unroll
@@ -117,15 +121,26 @@ expert_combine_kernel(const uint4 *__restrict__ recv, const float *__restrict__ 
                     ov[2 * h + 1] =
                         pack_bf16x2(__fmul_rn(__fmul_rn(hi.x, sc[i]), se), __fmul_rn(__fmul_rn(hi.y, sc[i]), se));
                 }
-                uint4 *o = y + row * H8 + 2 * pc;
-                st_v4(o, make_uint4(ov[0], ov[1], ov[2], ov[3]));
-                st_v4(o + 1, make_uint4(ov[4], ov[5], ov[6], ov[7]));
+                // fp8: into this warp's buffer; one bulk copy writes the unit
+                stage[2 * (pc - first)] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                stage[2 * (pc - first) + 1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
             } else {
                 uint32_t ov[4];
 #pragma unroll
                 for (int h = 0; h < 4; ++h)
                     ov[h] = pack_bf16x2(__fmul_rn(bf16_lo(wv[h]), se), __fmul_rn(bf16_hi(wv[h]), se));
                 st_v4(y + row * H8 + pc, make_uint4(ov[0], ov[1], ov[2], ov[3]));
+            }
+        }
+        if (FP8) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const unsigned n = min((unsigned)(32 * kSegTasks), pieces - first);
+                bulk_s2g(y + row * H8 + 2 * first, stage, n * 32);
+                bulk_commit();
+                bulk_wait_all();                          // the unit's rows are written ...
+                asm volatile("fence.proxy.async.global;" ::: "memory");   // ... and ordered before the flag
             }
         }
         __syncwarp();
@@ -215,13 +230,15 @@ int launch_expert_combine(const Dims &d, cudaStream_t st, const void *recv, cons
                           const float *topk_w, const int32_t *slot, void *out, unsigned *flags, unsigned epoch,
                           unsigned *status) {
     auto kernel = expert_combine_kernel<KMAX, FP8>;
-    static int resident = resident_blocks(kernel, kRBlock);      // blocks resident on the whole GPU
+    const size_t smem = FP8 ? (size_t)kRWarps * 32 * kSegTasks * 32 : 0;
+    static int resident = resident_blocks(kernel, kRBlock, smem);   // blocks resident on the whole GPU
     int grid = resident;
     if (d.max_blocks > 0 && d.max_blocks < grid) grid = d.max_blocks;
     if (grid < 2) return MOE_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)kRBlock);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;        // every block resident: consumers may wait on producers
