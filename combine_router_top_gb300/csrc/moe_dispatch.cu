@@ -324,7 +324,7 @@ dispatch_bf16_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restri
     bulk_wait_all();                         // every store complete before the grid ends
 }
 
-// ---- fused route finalisation + fp8 dispatch, for decode-sized batches ------
+// ---- fused route finalisation + dispatch, for decode-sized batches -----------
 //
 // The top-k kernel of moe_route leaves, per pair, its rank within its tile of
 // 32 tokens and, per tile, the count per expert. Here one block per token t
@@ -333,9 +333,9 @@ dispatch_bf16_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restri
 // starts), forms the slots of t's k choices while the copy is in flight
 // (slot_j = rank_j + the counts of expert e_j in the tiles before t's tile,
 // the tiles split over the block's threads), writes slot[] and recv_src,
-// quantises the row into shared memory and bulk-stores it to each kept
-// destination. Block 0 forms counts, offsets, rank_counts and dropped from
-// the tile counts.
+// then bulk-stores the row to each kept destination: quantised into shared
+// memory first for an fp8 dispatch, as staged for a bf16 one. Block 0 forms
+// counts, offsets, rank_counts and dropped from the tile counts.
 constexpr int kFusedMaxTiles = 32;             // decode-sized batches: at most 1024 tokens
 constexpr int kFusedThreads = 128;
 constexpr int kFusedMaxHidden = 16384;         // staged row + codes: 3 * H bytes of shared memory
@@ -374,8 +374,11 @@ __device__ void fused_totals(const int32_t *__restrict__ tile_counts, int n_tile
     }
 }
 
+// FP8: quantise the staged row and store codes and scales; bf16: store the
+// staged row itself to each kept destination.
+template <bool FP8>
 __global__ void __launch_bounds__(kFusedThreads)
-route_dispatch_fp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
+route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
                           const int32_t *__restrict__ rank, const int32_t *__restrict__ tile_counts,
                           int32_t *__restrict__ slot, uint8_t *__restrict__ recv_q, float *__restrict__ recv_scale,
                           int32_t *__restrict__ recv_src, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
@@ -438,6 +441,18 @@ route_dispatch_fp8_kernel(const uint16_t *__restrict__ x, const int32_t *__restr
         if (tid == 0) {
             atomicOr(status, kStatusWaitGaveUp);
             mbar_wait_bounded(&bar, 0);
+        }
+        return;
+    }
+    if constexpr (!FP8) {
+        // bf16: the staged row goes out as it is (recv_q holds bf16 rows here)
+        pdl_launch_dependents();
+        if (tid == 0) {
+            const int nd = s_n;
+            for (int j = 0; j < nd; ++j)
+                bulk_s2g(recv_q + (size_t)s_row[j] * H * 2, xs, (uint32_t)H * 2);
+            bulk_commit();
+            bulk_wait_all();
         }
         return;
     }
@@ -596,7 +611,7 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
     if (workspace_bytes < moe_route_dispatch_workspace_bytes(p)) return MOE_ERR_INVALID_ARG;
     const bool fp8 = d.dtype == MOE_DTYPE_FP8_E4M3_B128;
     const int n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
-    const bool fused = fp8 && d.H <= kFusedMaxHidden && n_tiles <= kFusedMaxTiles && d.max_blocks == 0;
+    const bool fused = d.H <= kFusedMaxHidden && n_tiles <= kFusedMaxTiles && d.max_blocks == 0;
     if (!fused) {
         rc = moe_route(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_counts, dropped, workspace,
                        workspace_bytes, stream);
@@ -604,11 +619,12 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
         return moe_dispatch(p, x, topk_idx, slot, recv, recv_scale, recv_src, stream);
     }
     // the same argument checks as moe_route and moe_dispatch
-    if (!counts || !offsets || !rank_counts || !dropped || !workspace || !recv_scale) return MOE_ERR_INVALID_ARG;
+    if (!counts || !offsets || !rank_counts || !dropped || !workspace) return MOE_ERR_INVALID_ARG;
+    if (fp8 != (recv_scale != nullptr)) return MOE_ERR_INVALID_ARG;
     if (d.T > 0 && (!logits || !x || !topk_idx || !topk_w || !slot || !recv || !recv_src)) return MOE_ERR_INVALID_ARG;
     const size_t logit_align = (d.E % 4 == 0) ? 16 : 4;
     if (!aligned(workspace, 16) || !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(rank_counts, 4) ||
-        !aligned(dropped, 4) || !aligned(recv_scale, 16))
+        !aligned(dropped, 4) || (fp8 && !aligned(recv_scale, 16)))
         return MOE_ERR_INVALID_ARG;
     if (d.T > 0 && (!aligned(logits, logit_align) || !aligned(x, 16) || !aligned(recv, 16) ||
                     !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(slot, 4) || !aligned(recv_src, 4)))
@@ -622,16 +638,17 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
         rc = launch_route_topk(d, st, logits, topk_idx, topk_w, rank, tile_counts);
         if (rc != MOE_OK) return rc;
     }
-    static bool smem_set[64] = {};
+    static bool smem_set[2][64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    if (!smem_set[dev]) {
-        if (cudaFuncSetAttribute(route_dispatch_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kernel = fp8 ? route_dispatch_kernel<true> : route_dispatch_kernel<false>;
+    if (!smem_set[fp8][dev]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  fused_smem_bytes(kFusedMaxHidden, kMaxExperts)) != cudaSuccess)
             return MOE_ERR_CUDA;
-        smem_set[dev] = true;
+        smem_set[fp8][dev] = true;
     }
-    if (launch_pdl_smem(route_dispatch_fp8_kernel, d.T + 1, kFusedThreads, fused_smem_bytes(d.H, d.E), st,
+    if (launch_pdl_smem(kernel, d.T + 1, kFusedThreads, fused_smem_bytes(d.H, d.E), st,
                         static_cast<const uint16_t *>(x), static_cast<const int32_t *>(topk_idx),
                         static_cast<const int32_t *>(rank), static_cast<const int32_t *>(tile_counts), slot,
                         static_cast<uint8_t *>(recv), recv_scale, recv_src, counts, offsets, rank_counts, dropped, d.H,

@@ -95,7 +95,7 @@ def test_edge_case_parity(case):
 
 
 FUSED = {
-    # fused kernel: fp8, H <= 16384, at most 32 tiles of 32 tokens
+    # fused kernel: H <= 16384, at most 32 tiles of 32 tokens
     "dsv3_fp8": W.WORKLOADS["dsv3_fp8"],
     "T1": W.WORKLOADS["dsv3_fp8"].with_(T=1),
     "T33": W.WORKLOADS["dsv3_fp8"].with_(T=33),
@@ -106,10 +106,14 @@ FUSED = {
     "H128_E1024": W.Workload("h128", T=70, H=128, E=1024, k=8, R=8, C=4, dtype=1, seed=34),
     "H16384": W.Workload("h16384", T=40, H=16384, E=32, k=4, R=4, C=16, dtype=1, seed=35),
     "H1152": W.Workload("h1152", T=64, H=1152, E=16, k=4, R=4, C=64, dtype=1, seed=33),
+    # bf16 dispatch: the staged row goes out as it is
+    "bf16_v2lite": W.WORKLOADS["v2lite"],
+    "bf16_T33_overflow": W.WORKLOADS["v2lite"].with_(T=33, C=2),
+    "bf16_H8_E1": W.Workload("h8e1", T=40, H=8, E=1, k=1, R=1, C=64, seed=37),
     # separate calls behind the same entry point
     "fallback_T1025": W.WORKLOADS["dsv3_fp8"].with_(T=1025, C=256),
     "fallback_H16512": W.Workload("h16512", T=20, H=16512, E=16, k=2, R=4, C=16, dtype=1, seed=36),
-    "fallback_bf16": W.WORKLOADS["v2lite"],
+    "fallback_bf16_T2048": W.WORKLOADS["v2lite"].with_(T=2048),
 }
 
 
