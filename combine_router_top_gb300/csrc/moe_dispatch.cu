@@ -454,54 +454,54 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
             bulk_commit();
             bulk_wait_all();
         }
-        return;
-    }
-    // 16 elements per task; the 8 tasks of a 128-element block sit in 8
-    // neighbouring lanes of one pass (the stride is a multiple of 8 and
-    // tasks % 8 == 0), so a pass is active or idle for a whole block
-    for (int pass = 0; pass < tasks; pass += kFusedThreads) {
-        const int task = pass + tid;
-        const bool on = task < tasks;
-        uint32_t wv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (on) {
-            const uint4 a = xs[2 * task], c = xs[2 * task + 1];
-            wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
-            wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
-        }
-        uint32_t m = 0;
-#pragma unroll
-        for (int h = 0; h < 8; ++h) m = bf16x2_absmax(m, wv[h]);
-        float amax = fmaxf(bf16_lo(m), bf16_hi(m));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
-        if (on) {
-            const float sc = e4m3_block_scale(amax);
-            uint32_t q[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc));
-                const uint32_t hi =
-                    pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc));
-                q[h] = lo | (hi << 16);
+    } else {
+        // 16 elements per task; the 8 tasks of a 128-element block sit in 8
+        // neighbouring lanes of one pass (the stride is a multiple of 8 and
+        // tasks % 8 == 0), so a pass is active or idle for a whole block
+        for (int pass = 0; pass < tasks; pass += kFusedThreads) {
+            const int task = pass + tid;
+            const bool on = task < tasks;
+            uint32_t wv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (on) {
+                const uint4 a = xs[2 * task], c = xs[2 * task + 1];
+                wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+                wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
             }
-            qs[task] = make_uint4(q[0], q[1], q[2], q[3]);
-            if ((task & 7) == 0) ss[task >> 3] = sc;
+            uint32_t m = 0;
+    #pragma unroll
+            for (int h = 0; h < 8; ++h) m = bf16x2_absmax(m, wv[h]);
+            float amax = fmaxf(bf16_lo(m), bf16_hi(m));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+            if (on) {
+                const float sc = e4m3_block_scale(amax);
+                uint32_t q[4];
+    #pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc));
+                    const uint32_t hi =
+                        pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc));
+                    q[h] = lo | (hi << 16);
+                }
+                qs[task] = make_uint4(q[0], q[1], q[2], q[3]);
+                if ((task & 7) == 0) ss[task >> 3] = sc;
+            }
         }
+        fence_proxy_async_smem();
+        __syncthreads();
+        const int nd = s_n;
+        if (tid == 0) {
+            for (int j = 0; j < nd; ++j) bulk_s2g(recv_q + (size_t)s_row[j] * H, qs, (uint32_t)H);
+            bulk_commit();
+        }
+        for (int i = tid; i < nd * nb; i += kFusedThreads) {
+            const int j = i / nb, blk = i - j * nb;
+            recv_scale[(size_t)s_row[j] * nb + blk] = ss[blk];
+        }
+        pdl_launch_dependents();
+        if (tid == 0) bulk_wait_all();
     }
-    fence_proxy_async_smem();
-    __syncthreads();
-    const int nd = s_n;
-    if (tid == 0) {
-        for (int j = 0; j < nd; ++j) bulk_s2g(recv_q + (size_t)s_row[j] * H, qs, (uint32_t)H);
-        bulk_commit();
-    }
-    for (int i = tid; i < nd * nb; i += kFusedThreads) {
-        const int j = i / nb, blk = i - j * nb;
-        recv_scale[(size_t)s_row[j] * nb + blk] = ss[blk];
-    }
-    pdl_launch_dependents();
-    if (tid == 0) bulk_wait_all();
 }
 
 template <int U>
