@@ -142,6 +142,29 @@ def test_expert_combine_rejects_bad_arguments_before_any_launch(moe):
     assert L.moe_expert_combine(C.byref(mk(moe, T=0)), *args, fake, fb, 1, None) == moe.MOE_OK
 
 
+def test_gemm_bf16_and_route_dispatch_argument_checks(moe):
+    L = moe.lib()
+    fake = C.c_void_p(1 << 40)
+    odd = C.c_void_p((1 << 40) + 8)
+    pb, pf = mk(moe, dtype=0), mk(moe)
+    args = [fake] * 4                                    # recv_x, counts, w, y
+    assert L.moe_expert_gemm_bf16(C.byref(pf), *args, None) == moe.MOE_ERR_UNSUPPORTED      # fp8 problem
+    assert L.moe_expert_gemm_bf16(C.byref(mk(moe, dtype=0, H=7168 + 8)), *args, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_expert_gemm_bf16(C.byref(pb), None, *args[1:], None) == moe.MOE_ERR_INVALID_ARG
+    for i in (0, 2, 3):                                  # recv_x, w, y need 16-byte alignment
+        a = list(args)
+        a[i] = odd
+        assert L.moe_expert_gemm_bf16(C.byref(pb), *a, None) == moe.MOE_ERR_INVALID_ARG
+    # moe_route_dispatch: a scale buffer exactly when the dispatch is fp8
+    ws = moe.moe_route_dispatch_workspace_bytes(pb)
+    a = [fake] * 12
+    a[10] = fake                                         # recv_scale given for a bf16 dispatch
+    assert L.moe_route_dispatch(C.byref(pb), *a, fake, ws, None) == moe.MOE_ERR_INVALID_ARG
+    a[10] = None                                         # and missing for an fp8 one
+    assert L.moe_route_dispatch(C.byref(pf), *a, fake, moe.moe_route_dispatch_workspace_bytes(pf), None) == \
+        moe.MOE_ERR_INVALID_ARG
+
+
 def test_calls_reject_bad_arguments_before_any_launch(moe):
     L = moe.lib()
     p = mk(moe)
