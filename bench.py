@@ -559,6 +559,8 @@ def run_ours(args, rank: int, world: int, local: int):
             "clocks": sampler.summary(t0, t1),
             "calls": per_call,
             "path_tokens_per_s": world * w.T / (step_ms_max * 1e-3),
+            "route_dispatch_combine_tokens_per_s":
+                world * w.T / (reduce_max(ms["route"] + ms["dispatch"] + ms["combine"], world, dev) * 1e-3),
             "pipelined": {"ms_per_step": pipe_ms, "tokens_per_s": world * w.T / (pipe_ms * 1e-3),
                           "what": "route, dispatch, expert, combine back to back (programmatic dependent "
                                   "launch), L2 flushed before each step"},
@@ -594,7 +596,8 @@ def run_dbo(args, dev) -> dict:
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     flush_r = torch.ones_like(flush_w)       # float32: the sum reduces in place, no widening copy
-    res = {"overlap_fraction": [], "step_ms": [], "dispatch_ub1_ms": [], "combine_ub0_ms": [], "serial_ms": []}
+    res = {"overlap_fraction": [], "step_ms": [], "dispatch_ub1_ms": [], "combine_ub0_ms": [], "overlap_ms": [],
+           "serial_ms": []}
     reps = 10
     with torch.cuda.stream(comp):
         for i in range(3 + reps):
@@ -603,7 +606,7 @@ def run_dbo(args, dev) -> dict:
             M.dbo_step(ctx, pf, x, lg, s, bufs, out, comp, comm, record_timing=True)
             t = M.dbo_read_timing(ctx)
             if i >= 3:
-                for key in ["overlap_fraction", "step_ms", "dispatch_ub1_ms", "combine_ub0_ms"]:
+                for key in ["overlap_fraction", "step_ms", "dispatch_ub1_ms", "combine_ub0_ms", "overlap_ms"]:
                     res[key].append(t[key])
         # the same work on one stream, for comparison
         for i in range(3 + reps):
@@ -629,6 +632,9 @@ def run_dbo(args, dev) -> dict:
             "single_stream_ms": med["serial_ms"], "dispatch_ub1_ms": med["dispatch_ub1_ms"],
             "combine_ub0_ms": med["combine_ub0_ms"],
             "overlapped_pair_bytes": bytes_dispatch(wd, kept1) + bytes_combine(wc, kept0),
+            # both kernels' algorithmic bytes over the window from the first's start to the last's end
+            "window_gbs": (bytes_dispatch(wd, kept1) + bytes_combine(wc, kept0))
+                          / ((med["dispatch_ub1_ms"] + med["combine_ub0_ms"] - med["overlap_ms"]) * 1e-3) / 1e9,
             "reps": reps, "l2": "flushed before every step"}
 
 
