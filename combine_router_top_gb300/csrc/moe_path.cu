@@ -16,8 +16,27 @@ extern "C" int moe_path_host(const moe_problem *p, const void *x_host, const flo
     int rc = check_problem(p, &d);
     if (rc != MOE_OK) return rc;
     if (bufs == nullptr) return MOE_ERR_INVALID_ARG;
-    if (d.T > 0 && (!x_host || !logits_host || !x_dev || !logits_dev || !out_dev || !out_host))
+    // every check the four calls make, before anything is enqueued, so that a
+    // failing call launches nothing
+    const moe_ubatch_bufs &c = *bufs;
+    const bool fp8 = d.dtype == MOE_DTYPE_FP8_E4M3_B128;
+    if (!c.counts || !c.offsets || !c.rank_counts || !c.dropped || !c.workspace || !s || !c.recv || !c.y)
         return MOE_ERR_INVALID_ARG;
+    if (c.workspace_bytes < moe_route_workspace_bytes(p) || fp8 != (c.recv_scale != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(c.counts, 4) || !aligned(c.offsets, 4) || !aligned(c.rank_counts, 4) || !aligned(c.dropped, 4) ||
+        !aligned(c.workspace, 16) || !aligned(s, 4) || !aligned(c.recv, 16) || !aligned(c.y, 16) ||
+        (fp8 && !aligned(c.recv_scale, 16)))
+        return MOE_ERR_INVALID_ARG;
+    if (d.T > 0) {
+        if (!x_host || !logits_host || !x_dev || !logits_dev || !out_dev || !out_host || !c.topk_idx || !c.topk_w ||
+            !c.slot || !c.recv_src)
+            return MOE_ERR_INVALID_ARG;
+        const size_t logit_align = (d.E % 4 == 0) ? 16 : 4;
+        if (!aligned(x_dev, 16) || !aligned(logits_dev, logit_align) || !aligned(out_dev, 16) ||
+            !aligned(c.topk_idx, 4) || !aligned(c.topk_w, 4) ||
+            !aligned(c.slot, 4) || !aligned(c.recv_src, 4))
+            return MOE_ERR_INVALID_ARG;
+    }
     cudaStream_t st = as_stream(stream);
     const size_t x_bytes = (size_t)d.T * d.H * sizeof(uint16_t);
     const size_t l_bytes = (size_t)d.T * d.E * sizeof(float);
@@ -26,15 +45,14 @@ extern "C" int moe_path_host(const moe_problem *p, const void *x_host, const flo
         if (cudaMemcpyAsync(logits_dev, logits_host, l_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
-    const moe_ubatch_bufs &b = *bufs;
-    rc = moe_route(p, logits_dev, b.topk_idx, b.topk_w, b.counts, b.offsets, b.slot, b.rank_counts, b.dropped,
-                   b.workspace, b.workspace_bytes, stream);
+    rc = moe_route(p, logits_dev, c.topk_idx, c.topk_w, c.counts, c.offsets, c.slot, c.rank_counts, c.dropped,
+                   c.workspace, c.workspace_bytes, stream);
     if (rc != MOE_OK) return rc;
-    rc = moe_dispatch(p, x_dev, b.topk_idx, b.slot, b.recv, b.recv_scale, b.recv_src, stream);
+    rc = moe_dispatch(p, x_dev, c.topk_idx, c.slot, c.recv, c.recv_scale, c.recv_src, stream);
     if (rc != MOE_OK) return rc;
-    rc = moe_expert_synthetic(p, b.recv, b.recv_scale, b.counts, s, b.y, stream);
+    rc = moe_expert_synthetic(p, c.recv, c.recv_scale, c.counts, s, c.y, stream);
     if (rc != MOE_OK) return rc;
-    rc = moe_combine(p, b.y, b.topk_idx, b.topk_w, b.slot, out_dev, stream);
+    rc = moe_combine(p, c.y, c.topk_idx, c.topk_w, c.slot, out_dev, stream);
     if (rc != MOE_OK) return rc;
     if (d.T > 0 && cudaMemcpyAsync(out_host, out_dev, x_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return MOE_ERR_CUDA;

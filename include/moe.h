@@ -1,8 +1,12 @@
 /*
  * moe.h -- C ABI of libmoe_gb300: the Mixture-of-Experts token path on one
  * NVIDIA GB300 (sm_103a): router top-k, per-expert count and scan, dispatch
- * into expert-major capacity-padded buffers, and top-k weighted combine, plus
- * a two-stream dual-batch-overlap step.
+ * into expert-major capacity-padded buffers, and top-k weighted combine; the
+ * experts between them as a synthetic stand-in or as grouped fp8 / bf16 GEMMs
+ * on the tensor cores; fused route + dispatch for decode batches; expert and
+ * combine with per-row readiness; a two-stream dual-batch-overlap step and its
+ * multi-layer schedule with CUDA-graph capture; and the whole path with host
+ * buffers in one call.
  *
  * Pages the operations follow (title, section):
  *   [PMC] "Efficient and portable mixture-of-experts communication"
@@ -78,8 +82,9 @@ typedef struct moe_problem {
     int32_t capacity;        /* C */
     int32_t dispatch_dtype;  /* moe_dispatch_dtype */
     int32_t max_blocks;      /* 0: library default grid; > 0: at most this many
-                                thread blocks for dispatch / expert / combine, so
-                                that kernels on another stream stay co-resident */
+                                thread blocks for dispatch / expert / combine and
+                                the persistent GEMM and readiness grids, so that
+                                kernels on another stream stay co-resident */
 } moe_problem;
 
 /* Human-readable name of a moe_status value. Never NULL; static storage. */
@@ -300,7 +305,10 @@ typedef struct moe_ubatch_bufs {
  * returns before the work completes: synchronise `stream` before reading
  * out_host or reusing x_host, logits_host or the device buffers. Two streams
  * with two buffer sets, used alternately, overlap one batch's copies with
- * the neighbouring batch's kernels. Errors as the four calls return them. */
+ * the neighbouring batch's kernels. Errors: MOE_ERR_INVALID_ARG for any
+ * argument one of the four calls would reject, or a null host buffer (when
+ * T > 0), checked before the first copy is enqueued, so a rejected call
+ * enqueues nothing; MOE_ERR_CUDA if a copy or launch fails. */
 int moe_path_host(const moe_problem *p, const void *x_host, const float *logits_host,
                   const float *s, void *x_dev, float *logits_dev,
                   const moe_ubatch_bufs *bufs, void *out_dev, void *out_host, void *stream);

@@ -190,6 +190,42 @@ def test_calls_reject_bad_arguments_before_any_launch(moe):
     assert L.dbo_read_timing(None, None) == moe.MOE_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("field", ["counts", "offsets", "rank_counts", "dropped", "workspace", "recv", "y",
+                                   "recv_scale", "topk_idx", "topk_w", "slot", "recv_src"])
+@pytest.mark.parametrize("how", ["null", "odd"])
+def test_path_host_checks_every_buffer_before_any_copy(moe, field, how):
+    """moe_path_host makes every check its four calls make before it enqueues
+    the first copy: one bad buffer fails the whole call with nothing launched."""
+    L = moe.lib()
+    p = mk(moe)
+    fake = 1 << 40
+    b = moe.moe_ubatch_bufs()
+    for n, _ in moe.moe_ubatch_bufs._fields_:
+        setattr(b, n, fake)
+    b.workspace_bytes = moe.moe_route_workspace_bytes(p)
+    setattr(b, field, None if how == "null" else fake + 2)
+    f = C.c_void_p(fake)
+    assert L.moe_path_host(C.byref(p), f, f, f, f, f, C.byref(b), f, f, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_path_host_rejects_small_workspace_and_null_host_buffers(moe):
+    L = moe.lib()
+    p = mk(moe)
+    fake = 1 << 40
+    b = moe.moe_ubatch_bufs()
+    for n, _ in moe.moe_ubatch_bufs._fields_:
+        setattr(b, n, fake)
+    b.workspace_bytes = moe.moe_route_workspace_bytes(p) - 1
+    f = C.c_void_p(fake)
+    assert L.moe_path_host(C.byref(p), f, f, f, f, f, C.byref(b), f, f, None) == moe.MOE_ERR_INVALID_ARG
+    b.workspace_bytes += 1
+    # x_host, logits_host, s, x_dev, logits_dev, bufs, out_dev, out_host: each one null
+    for i in range(8):
+        args = [f, f, f, f, f, C.byref(b), f, f]
+        args[i] = None
+        assert L.moe_path_host(C.byref(p), *args, None) == moe.MOE_ERR_INVALID_ARG, i
+
+
 def test_empty_batch_calls_are_noops_without_gpu(moe):
     """T == 0: dispatch and combine return MOE_OK without launching anything."""
     L = moe.lib()
