@@ -149,13 +149,7 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ top
             amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
             const float sc = e4m3_block_scale(amax);
             uint32_t q[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc));
-                const uint32_t hi =
-                    pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc));
-                q[h] = lo | (hi << 16);
-            }
+            quantise16_e4m3(wv, sc, q);
             qv[i] = make_uint4(q[0], q[1], q[2], q[3]);
             scale[i] = sc;
         }
@@ -199,7 +193,7 @@ constexpr int kTmaSeg = 1024;                    // fp8 unit: elements
 constexpr int kTmaFp8Threads = kTmaSeg / 16;     // one 16-element task per thread
 constexpr int kTmaBf16MaxRowBytes = 32768;       // bf16 rows staged whole (H <= 16384)
 
-__global__ void __launch_bounds__(kTmaFp8Threads)
+__global__ void __launch_bounds__(kTmaFp8Threads, 32)     // 32 CTAs (2048 threads) resident per SM
 dispatch_fp8_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
                         const int32_t *__restrict__ slot, uint8_t *__restrict__ recv_q,
                         float *__restrict__ recv_scale, int32_t *__restrict__ recv_src, int T, int H, int k,
@@ -257,13 +251,7 @@ dispatch_fp8_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restric
         amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
         const float sc = e4m3_block_scale(amax);
         uint32_t q[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc));
-            const uint32_t hi =
-                pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc));
-            q[h] = lo | (hi << 16);
-        }
+        quantise16_e4m3(wv, sc, q);
         qs[tid] = make_uint4(q[0], q[1], q[2], q[3]);
         if ((tid & 7) == 0) ss[tid >> 3] = sc;
         fence_proxy_async_smem();
@@ -477,13 +465,7 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
             if (on) {
                 const float sc = e4m3_block_scale(amax);
                 uint32_t q[4];
-    #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const uint32_t lo = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc));
-                    const uint32_t hi =
-                        pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc));
-                    q[h] = lo | (hi << 16);
-                }
+                quantise16_e4m3(wv, sc, q);
                 qs[task] = make_uint4(q[0], q[1], q[2], q[3]);
                 if ((task & 7) == 0) ss[task >> 3] = sc;
             }

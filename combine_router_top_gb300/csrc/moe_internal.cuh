@@ -283,6 +283,44 @@ __device__ __forceinline__ float e4m3_block_scale(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
+// Scales for which quantise16_e4m3 takes the FMA-corrected quotient.
+constexpr float kQuotientFastMin = 0x1p-100f, kQuotientFastMax = 0x1p120f;
+
+// The e4m3 codes of 16 bf16 elements of one block (wv: 8 bf16 pairs, lo
+// first) with block scale sc: code = e4m3(x / sc) of the IEEE fp32 quotient,
+// as four words of four codes. Inside [kQuotientFastMin, kQuotientFastMax]
+// (every finite scale of a block whose amax is at least about 2^-91) one
+// correctly rounded reciprocal r = 1/sc replaces the 16 divisions: per
+// element q0 = x*r, the remainder x - sc*q0 by FMA and one correction
+// q0 + rem*r (Markstein's FMA-based division: P. Markstein, IBM J. Res. Dev.
+// 34(1), 1990). That q can be one
+// fp32 ulp off the IEEE quotient, but never across an e4m3 rounding boundary:
+// an exhaustive host check over every bf16 amax whose scale is in the range
+// and every bf16 x with |x| <= amax finds the same code in every case. A zero
+// remainder keeps q0, which carries the sign of x (so -0 stays -0). Outside
+// the range (tiny blocks, an infinite amax, NaN) the IEEE division is used.
+__device__ __forceinline__ float fma_corrected_quotient(float x, float sc, float r) {
+    const float q0 = __fmul_rn(x, r);
+    const float rem = __fmaf_rn(-q0, sc, x);
+    return rem == 0.0f ? q0 : __fmaf_rn(rem, r, q0);
+}
+__device__ __forceinline__ void quantise16_e4m3(const uint32_t wv[8], float sc, uint32_t q[4]) {
+    if (sc >= kQuotientFastMin && sc <= kQuotientFastMax) {
+        const float r = __frcp_rn(sc);
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            q[h] = pack_e4m3x2(fma_corrected_quotient(bf16_lo(wv[2 * h]), sc, r),
+                               fma_corrected_quotient(bf16_hi(wv[2 * h]), sc, r)) |
+                   (pack_e4m3x2(fma_corrected_quotient(bf16_lo(wv[2 * h + 1]), sc, r),
+                                fma_corrected_quotient(bf16_hi(wv[2 * h + 1]), sc, r)) << 16);
+    } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            q[h] = pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h]), sc), __fdiv_rn(bf16_hi(wv[2 * h]), sc)) |
+                   (pack_e4m3x2(__fdiv_rn(bf16_lo(wv[2 * h + 1]), sc), __fdiv_rn(bf16_hi(wv[2 * h + 1]), sc)) << 16);
+    }
+}
+
 // Total order on fp32 logits as unsigned keys: larger logit -> larger key,
 // -0.0 folded onto +0.0, NaN mapped to 1 (below every number), 0 reserved
 // for "no candidate".

@@ -185,6 +185,38 @@ def test_fp8_zero_and_tiny_blocks():
     compare(g, o, w.C, True)
 
 
+
+def test_fp8_codes_over_every_bf16_value():
+    """The quantiser on every bf16 bit pattern, codes and scales bit-exact
+    against the oracle. Rows 0-63: all 65536 patterns sorted by magnitude, 128
+    to a block, so blocks of NaNs, infinities, subnormals and tiny values (the
+    IEEE-division path) sit beside blocks of one binade each (the
+    FMA-corrected path). Rows 64-127: blocks whose amax is a random finite
+    bf16 and whose other values are random patterns of either sign at or
+    below it, so x / sc spans the whole e4m3 range and below."""
+    from gpu_path import valid_rows
+    w = W.Workload("allbf16", T=128, H=1024, E=8, k=2, R=2, C=128, dtype=1, seed=25)
+    pats = np.arange(1 << 16, dtype=np.uint32)
+    order = np.lexsort((pats >> 15, pats & 0x7FFF))
+    x = np.empty((w.T, w.H), dtype=np.uint16)
+    x[:64] = pats[order].astype(np.uint16).reshape(64, w.H)
+    rng = np.random.default_rng(25)
+    blocks = x[64:].reshape(-1, 128)
+    for b in blocks:
+        amax = int(rng.integers(1, 0x7F80))
+        b[:] = rng.integers(0, amax + 1, size=128) | (rng.integers(0, 2, size=128) << 15)
+        b[int(rng.integers(0, 128))] = amax | (int(rng.integers(0, 2)) << 15)
+    g, o = run_both(w, x=x)
+    assert np.array_equal(g["slot"], o["slot"]) and int(o["dropped"]) == 0
+    e, r = valid_rows(o["counts"], w.C)
+    assert len(e) == w.T * w.k
+    assert np.array_equal(g["recv_src"][e, r], o["recv_src"][e, r])
+    assert np.array_equal(g["recv_q"][e, r], o["recv_q"][e, r]), "codes"
+    assert np.array_equal(g["recv_scale"][e, r].view(np.uint32), o["recv_scale"][e, r].view(np.uint32)), "scales"
+    # the two paths were both taken: infinite / tiny scales and ordinary ones
+    sc = o["recv_scale"][e, r]
+    assert np.isinf(sc).any() and (sc < 2.0**-100).any() and ((sc > 1e-3) & (sc < 1e3)).any()
+
 def test_nan_logits_give_in_range_distinct_indices():
     """NaN logits: the order is unspecified, but the indices stay valid."""
     from gpu_path import run_stages
