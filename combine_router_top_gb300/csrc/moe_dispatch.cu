@@ -182,9 +182,9 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ top
 //
 // fp8: a CTA of 64 threads takes a unit (token, 1024-element segment): one
 // bulk copy brings the 2 KB of bf16 into shared memory (mbarrier), each
-// thread quantises 16 elements into a shared-memory code row and the 8 scales,
-// and one thread issues, for every kept destination, a 1 KB bulk store of the
-// codes and a 32-byte bulk store of the scales. bf16: a warp takes a token:
+// thread quantises 16 elements in registers, and for every kept destination
+// the CTA writes the 1 KB of codes as one coalesced pass of 16-byte stores
+// and the 8 scales as 4-byte stores. bf16: a warp takes a token:
 // one bulk copy of the row in, one bulk store per destination out (each lane
 // j < k stores its own destination), no per-element instruction at all.
 // Both loop grid-stride over their units when max_blocks caps the grid.
@@ -199,7 +199,6 @@ dispatch_fp8_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restric
                         float *__restrict__ recv_scale, int32_t *__restrict__ recv_src, int T, int H, int k,
                         int C, unsigned *status) {
     __shared__ __align__(128) uint4 xs[kTmaSeg * 2 / 16];
-    __shared__ __align__(128) uint4 qs[kTmaSeg / 16];
     __shared__ __align__(16) float ss[kTmaSeg / 128];
     __shared__ __align__(8) uint64_t bar;
     __shared__ int s_row[kMaxTopK];
@@ -252,23 +251,19 @@ dispatch_fp8_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restric
         const float sc = e4m3_block_scale(amax);
         uint32_t q[4];
         quantise16_e4m3(wv, sc, q);
-        qs[tid] = make_uint4(q[0], q[1], q[2], q[3]);
         if ((tid & 7) == 0) ss[tid >> 3] = sc;
-        fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0) {
-            const int nd = s_n;
-            for (int j = 0; j < nd; ++j) {
-                const size_t row = (size_t)s_row[j];
-                bulk_s2g(recv_q + row * H + (size_t)seg * kTmaSeg, qs, kTmaSeg);
-                bulk_s2g(recv_scale + row * nb + (size_t)seg * (kTmaSeg / 128), ss, (kTmaSeg / 128) * 4);
-            }
-            bulk_commit();
-            bulk_wait_read_all();            // the codes and scales may be overwritten after this
-        }
-        __syncthreads();
+        // every thread stores its 16 codes to each kept destination (the CTA
+        // writes each destination's 1 KB in one coalesced pass), and thread
+        // 8j + b the scale of block b to destination j
+        const int nd = s_n;
+        const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+        for (int j = 0; j < nd; ++j)
+            st_v4(recv_q + (size_t)s_row[j] * H + (size_t)seg * kTmaSeg + (size_t)tid * 16, qv);
+        for (int i = tid; i < nd * (kTmaSeg / 128); i += kTmaFp8Threads)
+            recv_scale[(size_t)s_row[i >> 3] * nb + (size_t)seg * (kTmaSeg / 128) + (i & 7)] = ss[i & 7];
+        __syncthreads();                     // xs, ss and s_row are rewritten by the next unit
     }
-    if (tid == 0) bulk_wait_all();           // every store complete before the grid ends
 }
 
 __global__ void __launch_bounds__(32)

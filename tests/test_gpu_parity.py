@@ -74,6 +74,7 @@ EDGE = {
     "E1": W.Workload("E1", T=40, H=16, E=1, k=1, R=1, C=64, seed=8),
     "E6": W.Workload("E6", T=50, H=8, E=6, k=3, R=3, C=50, seed=9),
     "E1024_k16_fp8": W.Workload("E1024", T=100, H=128, E=1024, k=16, R=8, C=16, dtype=1, seed=10),
+    "k16_H2048_fp8": W.Workload("k16h2048", T=50, H=2048, E=64, k=16, R=4, C=50, dtype=1, seed=16),
     # hidden extremes
     "H8": W.Workload("H8", T=64, H=8, E=8, k=2, R=2, C=64, seed=11),
     "H65536": W.Workload("H65536", T=3, H=65536, E=4, k=2, R=2, C=4, seed=12),
