@@ -316,15 +316,17 @@ dispatch_bf16_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restri
 // starts), forms the slots of t's k choices while the copy is in flight
 // (slot_j = rank_j + the counts of expert e_j in the tiles before t's tile,
 // the tiles split over the block's threads), writes slot[] and recv_src,
-// then bulk-stores the row to each kept destination: quantised into shared
-// memory first for an fp8 dispatch, as staged for a bf16 one. Block 0 forms
+// then writes the row to each kept destination: for an fp8 dispatch each
+// thread stores the 16 codes it has just quantised (16-byte stores, coalesced
+// across the block), for a bf16 one the staged row leaves by one bulk store
+// per destination. Block 0 forms
 // counts, offsets, rank_counts and dropped from the tile counts.
 constexpr int kFusedMaxTiles = 32;             // decode-sized batches: at most 1024 tokens
 constexpr int kFusedThreads = 128;
-constexpr int kFusedMaxHidden = 16384;         // staged row + codes: 3 * H bytes of shared memory
+constexpr int kFusedMaxHidden = 16384;         // staged bf16 row: 2 * H bytes of shared memory
 
 constexpr size_t fused_smem_bytes(int H, int E) {
-    return 3 * (size_t)H > 4 * (size_t)E ? 3 * (size_t)H : 4 * (size_t)E;
+    return 2 * (size_t)H > 4 * (size_t)E ? 2 * (size_t)H : 4 * (size_t)E;
 }
 
 // tot: E ints of shared memory
@@ -367,7 +369,7 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
                           int32_t *__restrict__ recv_src, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                           int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped, int H, int E, int k,
                           int C, int R, int n_tiles, unsigned *status) {
-    // the bf16 row (2H bytes), then its codes (H bytes); block 0: the E totals
+    // the bf16 row (2H bytes); block 0: the E totals
     extern __shared__ __align__(128) uint4 fused_smem[];
     __shared__ float ss[kFusedMaxHidden / 128];
     __shared__ __align__(8) uint64_t bar;
@@ -384,7 +386,6 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
     const int t = blockIdx.x - 1;
     const int nb = H / 128, tasks = H / 16;
     uint4 *xs = fused_smem;
-    uint4 *qs = fused_smem + tasks * 2;
     if (tid == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
@@ -441,6 +442,7 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
         // 16 elements per task; the 8 tasks of a 128-element block sit in 8
         // neighbouring lanes of one pass (the stride is a multiple of 8 and
         // tasks % 8 == 0), so a pass is active or idle for a whole block
+        const int nd = s_n;
         for (int pass = 0; pass < tasks; pass += kFusedThreads) {
             const int task = pass + tid;
             const bool on = task < tasks;
@@ -461,23 +463,17 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
                 const float sc = e4m3_block_scale(amax);
                 uint32_t q[4];
                 quantise16_e4m3(wv, sc, q);
-                qs[task] = make_uint4(q[0], q[1], q[2], q[3]);
+                const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+                for (int j = 0; j < nd; ++j) st_v4(recv_q + (size_t)s_row[j] * H + (size_t)task * 16, qv);
                 if ((task & 7) == 0) ss[task >> 3] = sc;
             }
         }
-        fence_proxy_async_smem();
         __syncthreads();
-        const int nd = s_n;
-        if (tid == 0) {
-            for (int j = 0; j < nd; ++j) bulk_s2g(recv_q + (size_t)s_row[j] * H, qs, (uint32_t)H);
-            bulk_commit();
-        }
         for (int i = tid; i < nd * nb; i += kFusedThreads) {
             const int j = i / nb, blk = i - j * nb;
             recv_scale[(size_t)s_row[j] * nb + blk] = ss[blk];
         }
         pdl_launch_dependents();
-        if (tid == 0) bulk_wait_all();
     }
 }
 
