@@ -8,6 +8,8 @@ chained result, and bit-exact when the CUDA combine is given the oracle's own
 expert output and routing (both accumulate with one fp32 FMA per expert in
 selection order).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -217,6 +219,64 @@ def test_fp8_codes_over_every_bf16_value():
     # the two paths were both taken: infinite / tiny scales and ordinary ones
     sc = o["recv_scale"][e, r]
     assert np.isinf(sc).any() and (sc < 2.0**-100).any() and ((sc > 1e-3) & (sc < 1e3)).any()
+
+
+def _amax_x_chunks(blocks_per_chunk=1 << 17, H=7168):
+    """Every pair (amax, x) of bf16 values with |x| <= amax, for every positive
+    finite amax (subnormal ones included) and both signs of x, as 128-element
+    blocks: amax first, then 127 of its x values (zero-padded). Yields
+    [T, H] arrays of whole rows, blocks_per_chunk blocks at a time."""
+    per_row = H // 128
+    pending, n = [], 0
+    for a in range(1, 0x7F80):
+        v = np.arange(a + 1, dtype=np.uint16)
+        vals = np.concatenate([v, v | np.uint16(0x8000)])
+        vals = np.concatenate([vals, np.zeros(-len(vals) % 127, dtype=np.uint16)]).reshape(-1, 127)
+        b = np.empty((len(vals), 128), dtype=np.uint16)
+        b[:, 0] = a
+        b[:, 1:] = vals
+        pending.append(b)
+        n += len(b)
+        if n >= blocks_per_chunk or a == 0x7F7F:
+            blk = np.concatenate(pending)
+            blk = np.concatenate([blk, np.zeros((-len(blk) % per_row, 128), dtype=np.uint16)])
+            yield blk.reshape(-1, H)
+            pending, n = [], 0
+
+
+def test_fp8_quantiser_on_every_amax_x_pair():
+    """moe_dispatch quantises every (amax, x) pair of bf16 values, |x| <= amax,
+    x of either sign, amax over every positive finite bf16 (so blocks of
+    subnormal and tiny amax take the IEEE-division path and the rest the
+    FMA-corrected quotient): codes and scales bit-exact against the oracle's
+    dispatch of the same rows."""
+    import concurrent.futures as cf
+    import torch
+    import combine_router_top_gb300 as M
+    H = 7168
+
+    def expect(x):
+        T = x.shape[0]
+        q, sc, _ = O.dispatch_fp8(x, np.zeros((T, 1), np.int32), np.arange(T, dtype=np.int32).reshape(T, 1), 1, T)
+        return x, q[0], sc[0]
+
+    pairs = 0
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 2)) as ex:
+        for x, q_ref, sc_ref in ex.map(expect, _amax_x_chunks(H=H)):
+            T = x.shape[0]
+            p = M.problem(T, H, 1, 1, 1, T, M.MOE_DTYPE_FP8_E4M3_B128)
+            xd = torch.from_numpy(x.view(np.int16)).to("cuda:0")
+            idx = torch.zeros((T, 1), dtype=torch.int32, device="cuda:0")
+            sl = torch.arange(T, dtype=torch.int32, device="cuda:0").reshape(T, 1)
+            recv = torch.empty((T, H), dtype=torch.uint8, device="cuda:0")
+            scale = torch.empty((T, H // 128), dtype=torch.float32, device="cuda:0")
+            src = torch.empty((T,), dtype=torch.int32, device="cuda:0")
+            M.moe_dispatch(p, xd, idx, sl, recv, scale, src)
+            torch.cuda.synchronize()
+            assert np.array_equal(recv.cpu().numpy(), q_ref), "codes"
+            assert np.array_equal(scale.cpu().numpy().view(np.uint32), sc_ref.view(np.uint32)), "scales"
+            pairs += int((x.reshape(-1, 128)[:, 0] != 0).sum()) * 127
+    assert pairs > 10**9
 
 def test_nan_logits_give_in_range_distinct_indices():
     """NaN logits: the order is unspecified, but the indices stay valid."""
