@@ -178,48 +178,38 @@ dispatch_fp8_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ top
     }
 }
 
-// ---- TMA (bulk-copy) dispatch ----------------------------------------------
+// ---- segment (fp8) and bulk-copy (bf16) dispatch ------------------------------
 //
-// fp8: a CTA of 64 threads takes a unit (token, 1024-element segment): one
-// bulk copy brings the 2 KB of bf16 into shared memory (mbarrier), each
-// thread quantises 16 elements in registers, and for every kept destination
-// the CTA writes the 1 KB of codes as one coalesced pass of 16-byte stores
-// and the 8 scales as 4-byte stores. bf16: a warp takes a token:
-// one bulk copy of the row in, one bulk store per destination out (each lane
-// j < k stores its own destination), no per-element instruction at all.
+// fp8: a CTA of 64 threads takes a unit (token, 1024-element segment): each
+// thread loads its 16 elements with two 16-byte loads (2 KB, coalesced
+// across the CTA), quantises them in registers, and for every kept
+// destination the CTA writes the 1 KB of codes as one coalesced pass of
+// 16-byte stores and the 8 scales as 4-byte stores. bf16: a warp takes a
+// token: one bulk copy of the row in, one bulk store per destination out
+// (each lane j < k stores its own destination), no per-element instruction.
 // Both loop grid-stride over their units when max_blocks caps the grid.
 
-constexpr int kTmaSeg = 1024;                    // fp8 unit: elements
-constexpr int kTmaFp8Threads = kTmaSeg / 16;     // one 16-element task per thread
+constexpr int kFp8Seg = 1024;                    // fp8 unit: elements
+constexpr int kFp8SegThreads = kFp8Seg / 16;     // one 16-element task per thread
 constexpr int kTmaBf16MaxRowBytes = 32768;       // bf16 rows staged whole (H <= 16384)
 
-__global__ void __launch_bounds__(kTmaFp8Threads, 32)     // 32 CTAs (2048 threads) resident per SM
-dispatch_fp8_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
+__global__ void __launch_bounds__(kFp8SegThreads, 32)     // 32 CTAs (2048 threads) resident per SM
+dispatch_fp8_seg_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
                         const int32_t *__restrict__ slot, uint8_t *__restrict__ recv_q,
                         float *__restrict__ recv_scale, int32_t *__restrict__ recv_src, int T, int H, int k,
-                        int C, unsigned *status) {
-    __shared__ __align__(128) uint4 xs[kTmaSeg * 2 / 16];
-    __shared__ __align__(16) float ss[kTmaSeg / 128];
-    __shared__ __align__(8) uint64_t bar;
+                        int C) {
+    __shared__ __align__(16) float ss[kFp8Seg / 128];
     __shared__ int s_row[kMaxTopK];
     __shared__ int s_n;
     pdl_enter();
     const int tid = threadIdx.x, lane = tid & 31;
-    const int segs = H / kTmaSeg, nb = H / 128;
+    const int segs = H / kFp8Seg, nb = H / 128;
     const long long units = (long long)T * segs;
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    unsigned phase = 0;
-    for (long long u = blockIdx.x; u < units; u += gridDim.x, phase ^= 1u) {
+    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
         const int t = (int)(u / segs), seg = (int)(u % segs);
-        if (tid == 0) {
-            fence_proxy_async_smem();                // earlier generic reads of xs before the bulk write
-            mbar_expect_tx(&bar, kTmaSeg * 2);
-            bulk_g2s(xs, x + (size_t)t * H + (size_t)seg * kTmaSeg, kTmaSeg * 2, &bar);
-        }
+        // the 16 elements of task tid: two 16-byte loads, coalesced across the CTA
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H + (size_t)seg * kFp8Seg) + 2 * tid;
+        const uint4 a = ld_stream_v4(src), c = ld_stream_v4(src + 1);
         if (tid < 32) {
             const int dest = load_dest(t, k, C, topk_idx, slot);
             const unsigned kept = __ballot_sync(kFull, dest >= 0);
@@ -229,17 +219,7 @@ dispatch_fp8_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restric
             }
             if (lane == 0) s_n = __popc(kept);
         }
-        const bool ok = mbar_wait_bounded(&bar, phase);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                atomicOr(status, kStatusWaitGaveUp);
-                mbar_wait_bounded(&bar, phase);          // the load in flight, bounded again
-                bulk_wait_all();
-            }
-            return;
-        }
-        // quantise the 16 elements of task tid (lanes 8g .. 8g+7 share a 128-element block)
-        const uint4 a = xs[2 * tid], c = xs[2 * tid + 1];
+        // quantise the 16 elements (lanes 8g .. 8g+7 share a 128-element block)
         const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
         uint32_t m = 0;
 #pragma unroll
@@ -259,10 +239,10 @@ dispatch_fp8_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restric
         const int nd = s_n;
         const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
         for (int j = 0; j < nd; ++j)
-            st_v4(recv_q + (size_t)s_row[j] * H + (size_t)seg * kTmaSeg + (size_t)tid * 16, qv);
-        for (int i = tid; i < nd * (kTmaSeg / 128); i += kTmaFp8Threads)
-            recv_scale[(size_t)s_row[i >> 3] * nb + (size_t)seg * (kTmaSeg / 128) + (i & 7)] = ss[i & 7];
-        __syncthreads();                     // xs, ss and s_row are rewritten by the next unit
+            st_v4(recv_q + (size_t)s_row[j] * H + (size_t)seg * kFp8Seg + (size_t)tid * 16, qv);
+        for (int i = tid; i < nd * (kFp8Seg / 128); i += kFp8SegThreads)
+            recv_scale[(size_t)s_row[i >> 3] * nb + (size_t)seg * (kFp8Seg / 128) + (i & 7)] = ss[i & 7];
+        __syncthreads();                     // ss and s_row are rewritten by the next unit
     }
 }
 
@@ -528,14 +508,13 @@ extern "C" int moe_dispatch(const moe_problem *p, const void *x, const int32_t *
     cudaStream_t st = as_stream(stream);
     unsigned *status = device_status_word();
     if (status == nullptr) return MOE_ERR_CUDA;
-    if (fp8 && d.H % kTmaSeg == 0) {
-        static int resident = resident_blocks(dispatch_fp8_tma_kernel, kTmaFp8Threads);
-        const long long units = (long long)d.T * (d.H / kTmaSeg);
+    if (fp8 && d.H % kFp8Seg == 0) {
+        static int resident = resident_blocks(dispatch_fp8_seg_kernel, kFp8SegThreads);
+        const long long units = (long long)d.T * (d.H / kFp8Seg);
         const int grid = d.max_blocks > 0 ? persistent_grid(units, resident, d.max_blocks)
                                           : (int)std::min<long long>(units, 1LL << 30);
-        if (launch_pdl(dispatch_fp8_tma_kernel, grid, kTmaFp8Threads, st, static_cast<const uint16_t *>(x), topk_idx,
-                       slot, static_cast<uint8_t *>(recv), recv_scale, recv_src, d.T, d.H, d.k, d.C, status) !=
-            cudaSuccess)
+        if (launch_pdl(dispatch_fp8_seg_kernel, grid, kFp8SegThreads, st, static_cast<const uint16_t *>(x), topk_idx,
+                       slot, static_cast<uint8_t *>(recv), recv_scale, recv_src, d.T, d.H, d.k, d.C) != cudaSuccess)
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
