@@ -96,6 +96,7 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+NOMINAL_HBM_GBS = 7900.0      # HBM3e data-sheet rate, for context beside the measured copy peak
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_PER_BF16 = 2.0            # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 
@@ -535,7 +536,8 @@ def run_ours(args, rank: int, world: int, local: int):
                  ("expert", lambda: bytes_expert(w, kept)), ("combine", lambda: cb)]:
         by = f()
         per_call[n] = {"us": 1e3 * ms[n], "algorithmic_bytes": by, "gbs": by / (ms[n] * 1e-3) / 1e9,
-                       "frac": by / (ms[n] * 1e-3) / 1e9 / peak}
+                       "frac": by / (ms[n] * 1e-3) / 1e9 / peak,
+                       "frac_of_nominal": by / (ms[n] * 1e-3) / 1e9 / NOMINAL_HBM_GBS}
     line = None
     if rank == 0:
         achieved = cb / (comb_ms * 1e-3) / 1e9
@@ -546,7 +548,8 @@ def run_ours(args, rank: int, world: int, local: int):
             "roofline": {"kernel": "combine_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
                          "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                          "traffic": ncu_traffic("combine", WORKLOAD),
-                         "algorithmic_bytes": cb},
+                         "algorithmic_bytes": cb, "nominal_gbs": NOMINAL_HBM_GBS,
+                         "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
             "e2e": {"value": world * w.T / (e2e_ms * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": x.numel() * 2 + lg.numel() * 4, "d2h_bytes_per_step": out.numel() * 2,
                     "ms_per_step": e2e_ms,
