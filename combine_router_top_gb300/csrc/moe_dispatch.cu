@@ -10,12 +10,19 @@
 // the expert's rows of this HBM, at the address the slot fixes; no counts have
 // to be awaited because moe_route already produced them.
 //
-// Persistent kernels: one wave of resident thread blocks; every warp walks
-// its own work units (token, segment of its row) with no block-wide barrier.
-// Lanes j < k hold the token's destination rows and broadcast them by
-// shuffle (ascending j). The next unit's routing and row data are loaded
-// before the current unit is stored, so that two units' loads are in flight.
-// recv_src is written on a token's first segment.
+// Kernels, chosen by moe_dispatch from the dtype and H:
+//   fp8, H % 1024 == 0: dispatch_fp8_seg, one 64-thread CTA per (token,
+//     1024-element segment), loads and stores straight from registers;
+//   bf16, rows of at most 32 KB: dispatch_bf16_tma, one warp per token, one
+//     bulk copy in and one bulk copy out per destination;
+//   otherwise the persistent register kernels below: one wave of resident
+//     thread blocks, every warp walking its own work units (token, segment of
+//     its row) with no block-wide barrier, the next unit's routing and row
+//     data loaded before the current unit is stored.
+// In all of them lanes j < k hold the token's destination rows (ascending j)
+// and recv_src is written once per kept pair. moe_route_dispatch fuses the
+// slot computation of moe_route into the fp8 and bf16 dispatch for decode
+// batches (route_dispatch_kernel, at the end of this file).
 #include <algorithm>
 
 #include "moe_internal.cuh"
