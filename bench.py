@@ -36,6 +36,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -126,10 +127,15 @@ def x_of(w: W.Workload):
 
 
 def kernel_source_sha(files) -> str:
+    """sha256[:16] of the kernels' code: the sources with comments and
+    whitespace removed, so that an edit to a comment keeps a record valid."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "combine_router_top_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "combine_router_top_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

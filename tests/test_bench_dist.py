@@ -52,3 +52,18 @@ def test_single_rank_is_identity():
     import bench
     assert bench.reduce_max(3.25, 1) == 3.25
     bench.barrier(1)
+
+
+def test_traffic_records_follow_code_not_comments(tmp_path, monkeypatch):
+    """A recorded ncu traffic figure stays valid through comment edits and
+    lapses when the kernel's code changes."""
+    import bench
+    csrc = tmp_path / "combine_router_top_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (csrc / "k.cu").write_text("// kernel\n__global__ void k(int *p) { p[0] = 1; }\n")
+    a = bench.kernel_source_sha(["k.cu"])
+    (csrc / "k.cu").write_text("/* the\n kernel */\n__global__ void k(int *p)\n{\n    p[0] = 1;   // store\n}\n")
+    assert bench.kernel_source_sha(["k.cu"]) == a
+    (csrc / "k.cu").write_text("__global__ void k(int *p) { p[0] = 2; }\n")
+    assert bench.kernel_source_sha(["k.cu"]) != a
