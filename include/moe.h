@@ -182,11 +182,11 @@ int moe_dispatch(const moe_problem *p, const void *x,
 /* moe_route followed by moe_dispatch in one call, with the same outputs bit
  * for bit, for decode: [PMC §Dispatch] counts tokens per destination inside
  * the dispatch kernel. For at most 1024 tokens, H <= 16384 and
- * max_blocks == 0 (fp8 or bf16 dispatch), it runs in two launches instead of three: the
- * route's top-k kernel, then one kernel with a block per token that forms the
- * token's slots from the per-tile counts and dispatches its row (launched as
- * a programmatic dependent of the first). Otherwise it calls moe_route and
- * moe_dispatch. workspace: device scratch of at least
+ * max_blocks == 0 (fp8 or bf16 dispatch), it runs in two launches instead of
+ * three: the route's top-k kernel, then one kernel with a block per token
+ * that forms the token's slots from the per-tile counts and dispatches its
+ * row (launched as a programmatic dependent of the first). Otherwise it calls
+ * moe_route and moe_dispatch. workspace: device scratch of at least
  * moe_route_dispatch_workspace_bytes(p) bytes, 16-byte aligned, contents
  * needing no initialisation, not shared with a concurrent call. */
 size_t moe_route_dispatch_workspace_bytes(const moe_problem *p);
