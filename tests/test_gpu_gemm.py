@@ -206,11 +206,16 @@ CASES_BF16 = {
     "H512_two_row_tiles": (W.Workload("b512", T=150, H=512, E=2, k=2, R=1, C=160, seed=303), None),
     "H2048": (W.Workload("b2048", T=24, H=2048, E=2, k=2, R=2, C=32, seed=304), None),
     "overflow_and_empty": (W.Workload("bov", T=64, H=256, E=8, k=2, R=4, C=8, seed=305), [2, 5]),
+    # about 300 rows per expert: three 128-row tiles, the last one ragged
+    "H256_three_row_blocks": (W.Workload("b300", T=300, H=256, E=2, k=2, R=1, C=320, seed=306), None),
 }
 
 
+@pytest.mark.parametrize("max_blocks", [0, 1, 3])
 @pytest.mark.parametrize("case", sorted(CASES_BF16))
-def test_gemm_bf16_matches_oracle(case):
+def test_gemm_bf16_matches_oracle(case, max_blocks):
+    """Small grids (one CTA, three CTAs) walk many tiles per CTA, so the two
+    TMEM accumulators alternate and are reused across tiles within one CTA."""
     import combine_router_top_gb300 as M
     w, empty = CASES_BF16[case]
     rx, counts = oracle_dispatch_bf16(w)
@@ -224,7 +229,7 @@ def test_gemm_bf16_matches_oracle(case):
     for e in range(w.E):                      # rows past the count: garbage bits, NaNs included
         kept = min(int(counts[e]), w.C)
         rx_dev[e, kept:] = rng.integers(0, 1 << 16, size=(w.C - kept, w.H), dtype=np.uint16)
-    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, M.MOE_DTYPE_BF16)
+    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, M.MOE_DTYPE_BF16, max_blocks)
     y = torch.full((w.E, w.C, w.H), SENTINEL, dtype=torch.int32, device=DEV).to(torch.int16)
     M.moe_expert_gemm_bf16(p, torch.from_numpy(rx_dev.view(np.int16)).to(DEV),
                            torch.from_numpy(np.ascontiguousarray(counts, dtype=np.int32)).to(DEV),
@@ -238,7 +243,7 @@ def test_gemm_bf16_matches_oracle(case):
         assert np.all(yh[e, kept:] == SENTINEL), f"expert {e}: rows past the count were written"
         for r in range(kept):
             worst = max(worst, check_row_bf16(yh[e, r], y_ref[e, r], rx[e, r], wb[e]))
-    print(f"bf16 {case}: max |err| / S = {worst:.3g}")
+    print(f"bf16 {case} max_blocks={max_blocks}: max |err| / S = {worst:.3g}")
 
 
 @pytest.mark.parametrize("name", ["v2lite", "dbo_prefill"])
