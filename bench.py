@@ -588,6 +588,69 @@ def run_ours(args, rank: int, world: int, local: int):
     return line, dev
 
 
+def run_all_configs(args, dev, reps: int = 20) -> dict:
+    """Route, dispatch, expert stand-in and combine of every configuration,
+    each call isolated (L2 flushed before it) and event-timed on its stream;
+    the dual-batch configuration is timed per micro-batch (half its tokens).
+    Parity of each configuration is the GPU test suite's, not this run's."""
+    import torch
+    import combine_router_top_gb300 as M
+    peak, peak_kind = measured_peak()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones_like(flush_w)
+    stream = torch.cuda.current_stream()
+    rows = []
+    for name in ["tiny", "v2lite", "mixtral_skew", "dsv3_fp8", "dbo"]:
+        w = W.WORKLOADS[name]
+        if name == "dbo":
+            w = w.with_(T=w.T // 2)
+        p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
+        x = torch.from_numpy(x_of(w).view(np.int16)).to(dev)
+        lg = torch.from_numpy(W.make_logits(w)).to(dev)
+        s = torch.from_numpy(W.expert_scale(w)).to(dev)
+        b = M.alloc_buffers(p, dev)
+        out = torch.empty((w.T, w.H), dtype=torch.int16, device=dev)
+        calls = [
+            ("route", lambda: M.moe_route(p, lg, b["topk_idx"], b["topk_w"], b["counts"], b["offsets"], b["slot"],
+                                          b["rank_counts"], b["dropped"], b["workspace"], stream)),
+            ("dispatch", lambda: M.moe_dispatch(p, x, b["topk_idx"], b["slot"], b["recv"], b.get("recv_scale"),
+                                                b["recv_src"], stream)),
+            ("expert", lambda: M.moe_expert_synthetic(p, b["recv"], b.get("recv_scale"), b["counts"], s, b["y"],
+                                                      stream)),
+            ("combine", lambda: M.moe_combine(p, b["y"], b["topk_idx"], b["topk_w"], b["slot"], out, stream)),
+        ]
+        times = {n: [] for n, _ in calls}
+        for i in range(3 + reps):
+            for n, fn in calls:
+                flush_w.fill_(1)
+                flush_r.sum()
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                z.record(stream)
+                if i >= 3:
+                    times[n].append((a, z))
+        torch.cuda.synchronize()
+        kept = w.T * w.k - int(b["dropped"].item())
+        by = {"route": bytes_route(w), "dispatch": bytes_dispatch(w, kept), "expert": bytes_expert(w, kept),
+              "combine": bytes_combine(w, kept)}
+        us = {n: 1e3 * statistics.median(a.elapsed_time(z) for a, z in v) for n, v in times.items()}
+        row = {"workload": name if name != "dbo" else "dbo (one micro-batch)", "T": w.T, "H": w.H, "E": w.E,
+               "top_k": w.k, "R": w.R, "C": w.C,
+               "dispatch_dtype": "fp8_e4m3_b128" if w.dtype == W.DTYPE_FP8_E4M3_B128 else "bf16",
+               "kept_pairs": kept, "dropped": w.T * w.k - kept,
+               "dispatch_combine_tokens_per_s": w.T / ((us["dispatch"] + us["combine"]) * 1e-6)}
+        for n in us:
+            row[n] = {"us": us[n], "algorithmic_bytes": by[n], "gbs": by[n] / (us[n] * 1e-6) / 1e9,
+                      "frac": by[n] / (us[n] * 1e-6) / 1e9 / peak}
+        rows.append(row)
+        del b, x, out
+        torch.cuda.empty_cache()
+    return {"peak_gbs": peak, "peak_source": f"{peak_kind} hbm_gbs", "reps": reps,
+            "l2": "flushed before every call", "configs": rows}
+
+
 def run_dbo(args, dev) -> dict:
     """Dual-batch-overlap step on the 8192-token prefill workload."""
     import torch
@@ -847,10 +910,22 @@ def main():
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--gemm-only", action="store_true", help="only the grouped GEMM measurement")
     ap.add_argument("--gemm-experts", type=int, default=0, help="with --gemm-only: E experts (profiling case)")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="only the per-configuration timings of route, dispatch, expert and combine")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.all_configs:
+        import torch
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        from combine_router_top_gb300 import build as B
+        import combine_router_top_gb300 as M
+        if not os.path.exists(M.LIB_PATH):
+            B.build()
+        print(json.dumps({"all_configs": run_all_configs(args, dev)}), flush=True)
         return
     if args.gemm_only:
         import torch
