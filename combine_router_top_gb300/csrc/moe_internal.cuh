@@ -18,6 +18,12 @@
 namespace moe {
 
 constexpr int kTileTokens = 32;    // tokens per route tile: one 32-bit mask word per expert
+constexpr int kChunkTiles = 32;    // route tiles per chunk of the two-level scan of tile counts
+
+// The route finaliser sums the counts of all earlier tiles directly, about
+// n_tiles^2 * E / 2 loads in all; above 2^22 of them (128 tiles at E = 256)
+// the two-level scan, two launches more but linear, is faster.
+inline bool route_two_level(size_t n_tiles, int E) { return n_tiles * n_tiles * (size_t)E > ((size_t)1 << 22); }
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxHidden = 65536;

@@ -19,6 +19,11 @@
 //      sum of the earlier tiles' counts; slot = base + rank in tile, or -1 at
 //      or past the capacity. The last CTA also forms the totals, offsets,
 //      rank counts and drops.
+// The sum over earlier tiles grows with the square of the batch; once it is
+// large (route_two_level), two more launches between K1 and K2 make it a
+// two-level scan: route_chunk_sums adds each chunk of kChunkTiles tiles,
+// route_chunk_scan turns the chunk sums into exclusive bases, and K2 adds to
+// its chunk's base only the tiles before it in its own chunk.
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -101,13 +106,57 @@ route_topk_tile_kernel(const float *__restrict__ logits, int T, int E, int k,
         tile_counts[(size_t)tile * E + e] = __popc(mask[e]);
 }
 
+// Chunk c of kChunkTiles tiles: chunk_sums[c][e] = the sum of its tiles'
+// counts of expert e.
+__global__ void __launch_bounds__(1024)
+route_chunk_sums_kernel(int n_tiles, int E, const int32_t *__restrict__ tile_counts, int32_t *__restrict__ chunk_sums) {
+    pdl_enter();
+    const int c = blockIdx.x;
+    const int t0 = c * kChunkTiles, t1 = min(n_tiles, t0 + kChunkTiles);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int s = 0;
+#pragma unroll 8
+        for (int t = t0; t < t1; ++t) s += __ldg(tile_counts + (size_t)t * E + e);
+        chunk_sums[(size_t)c * E + e] = s;
+    }
+}
+
+// One CTA: chunk_base[c][e] = the sum of chunk_sums[c'][e] over c' < c.
+// 1024 / E thread groups split the chunks into contiguous ranges; each group
+// starts from the sums of the groups before it.
+__global__ void __launch_bounds__(1024)
+route_chunk_scan_kernel(int n_chunks, int E, const int32_t *__restrict__ chunk_sums, int32_t *__restrict__ chunk_base) {
+    __shared__ int32_t part[1024];
+    pdl_enter();
+    const int G = (1024 / E) > 0 ? (1024 / E) : 1;
+    const int tid = threadIdx.x, g = tid / E, e = tid % E;
+    const int per = (n_chunks + G - 1) / G;
+    const int c0 = g * per, c1 = min(n_chunks, c0 + per);
+    if (g < G) {
+        int s = 0;
+        for (int c = c0; c < c1; ++c) s += chunk_sums[(size_t)c * E + e];
+        part[tid] = s;
+    }
+    __syncthreads();
+    if (g < G) {
+        int run = 0;
+        for (int gg = 0; gg < g; ++gg) run += part[gg * E + e];
+        for (int c = c0; c < c1; ++c) {
+            chunk_base[(size_t)c * E + e] = run;
+            run += chunk_sums[(size_t)c * E + e];
+        }
+    }
+}
+
 // CTA b finalises tile b: its per-expert base is the sum of the counts of
 // tiles 0..b-1 (read from the workspace; 1024/E thread groups split the
-// tiles), slot = base + rank in tile (or -1 at or past C). The last CTA also
+// tiles), or with chunk_base its chunk's base plus the tiles before b in the
+// chunk; slot = base + rank in tile (or -1 at or past C). The last CTA also
 // adds its own tile to get the totals and writes counts, offsets,
 // rank_counts and dropped.
 __global__ void __launch_bounds__(1024, 1)
 route_finalize_kernel(int T, int n_tiles, int E, int k, int R, int C, const int32_t *__restrict__ tile_counts,
+                      const int32_t *__restrict__ chunk_base,
                       const int32_t *__restrict__ topk_idx, int32_t *__restrict__ slot,
                       int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                       int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped) {
@@ -122,10 +171,11 @@ route_finalize_kernel(int T, int n_tiles, int E, int k, int R, int C, const int3
     const bool last = b == (int)gridDim.x - 1;
     const int G = (1024 / E) > 0 ? (1024 / E) : 1;
     const int g = tid / E, e = tid % E;
+    const int from = chunk_base != nullptr ? b / kChunkTiles * kChunkTiles : 0;
     if (g < G) {
         int s = 0;
 #pragma unroll 8
-        for (int tt = g; tt < b; tt += G) s += __ldg(tile_counts + (size_t)tt * E + e);
+        for (int tt = from + g; tt < b; tt += G) s += __ldg(tile_counts + (size_t)tt * E + e);
         part[tid] = s;
     }
     if (last) {
@@ -134,7 +184,7 @@ route_finalize_kernel(int T, int n_tiles, int E, int k, int R, int C, const int3
     }
     __syncthreads();
     if (tid < E) {
-        int s = 0;
+        int s = chunk_base != nullptr ? chunk_base[(size_t)(b / kChunkTiles) * E + tid] : 0;
         for (int gg = 0; gg < G; ++gg) s += part[gg * E + tid];
         base[tid] = s;
     }
@@ -240,12 +290,27 @@ extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *top
         else e = launch_topk<32>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
+    // many tiles: the two-level scan of the tile counts (chunk sums, then
+    // their exclusive bases), each kernel a programmatic dependent of the last
+    const int32_t *chunk_base = nullptr;
+    if (route_two_level((size_t)n_tiles, d.E)) {
+        const int n_chunks = (n_tiles + kChunkTiles - 1) / kChunkTiles;
+        int32_t *sums = wc + (size_t)n_tiles * d.E;
+        int32_t *bases = sums + (size_t)n_chunks * d.E;
+        const int threads = d.E < 1024 ? (d.E + 31) / 32 * 32 : 1024;
+        if (launch_pdl(route_chunk_sums_kernel, n_chunks, threads, st, n_tiles, d.E,
+                       static_cast<const int32_t *>(wc), sums) != cudaSuccess ||
+            launch_pdl(route_chunk_scan_kernel, 1, 1024, st, n_chunks, d.E, static_cast<const int32_t *>(sums),
+                       bases) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        chunk_base = bases;
+    }
     // an empty batch still runs one finalise block: it writes the zero counts.
-    // Launched as a programmatic dependent of the top-k kernel: its launch
-    // latency overlaps the top-k kernel's run.
+    // Launched as a programmatic dependent of the kernel before it: its launch
+    // latency overlaps that kernel's run.
     if (launch_pdl(route_finalize_kernel, n_tiles > 0 ? n_tiles : 1, 1024, st, d.T, n_tiles, d.E, d.k, d.R, d.C,
-                   static_cast<const int32_t *>(wc), static_cast<const int32_t *>(topk_idx), slot, counts, offsets,
-                   rank_counts, dropped) != cudaSuccess)
+                   static_cast<const int32_t *>(wc), chunk_base, static_cast<const int32_t *>(topk_idx), slot,
+                   counts, offsets, rank_counts, dropped) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

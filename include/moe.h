@@ -105,7 +105,10 @@ int moe_validate(const moe_problem *p);
 
 /* Bytes of device workspace moe_route needs for this problem (host-only, no
  * CUDA call); 0 if the problem is invalid. The workspace holds one 32-bit
- * count per (tile of 32 tokens, expert). Its contents need no initialisation. */
+ * count per (tile of 32 tokens, expert) and, for large batches (more than
+ * 2^22 / E tiles squared: 4096 tokens at E = 256), two 32-bit values per
+ * (chunk of 32 tiles, expert) for a two-level scan of those counts. Its
+ * contents need no initialisation. */
 size_t moe_route_workspace_bytes(const moe_problem *p);
 
 /* Step 1 and 2: router top-k with renormalised softmax weights, then the
@@ -146,8 +149,8 @@ int moe_route(const moe_problem *p, const float *logits,
  *  Scratch: a 1 MiB array in device memory, defined in the library, which
  *  every GPU that loads the library holds until the process exits. The call
  *  returns MOE_ERR_UNSUPPORTED, launching nothing, when the problem needs more
- *  (moe_route_workspace_bytes(p) > 1 MiB: 32 tokens x E experts x 4 bytes per
- *  tile of 32 tokens; for instance more than 32768 tokens at E = 256).
+ *  (moe_route_workspace_bytes(p) > 1 MiB, about E x 4.25 bytes per tile of 32
+ *  tokens; for instance more than 30784 tokens at E = 256).
  *  Set-up: the first call on a device looks up the array's device address
  *  with that device current (cudaGetSymbolAddress); make that first call
  *  before any stream capture on the device. Later calls do no CUDA call other

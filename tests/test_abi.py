@@ -84,6 +84,14 @@ def test_validate_accepts_workloads(moe):
 def test_route_workspace_bytes(moe):
     p = mk(moe)        # 1024 tokens -> 32 tiles of 32, 256 experts, int32
     assert moe.moe_route_workspace_bytes(p) == 32 * 256 * 4
+    # while tiles^2 * E <= 2^22 the finaliser sums earlier tiles directly (128
+    # tiles at E = 256); beyond, the two-level scan adds a sum and a base per
+    # (chunk of 32 tiles, expert)
+    assert moe.moe_route_workspace_bytes(mk(moe, T=4096)) == 128 * 256 * 4
+    assert moe.moe_route_workspace_bytes(mk(moe, T=4097)) == (129 + 2 * 5) * 256 * 4
+    # rounded up to a multiple of 256 bytes
+    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=500, k=5, R=4)) == ((102 + 2 * 4) * 500 * 4 + 255) // 256 * 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=100, k=5, R=4)) == (102 * 100 * 4 + 255) // 256 * 256
     assert moe.moe_route_workspace_bytes(mk(moe, T=0)) == 256
     assert moe.moe_route_workspace_bytes(mk(moe, T=33, E=8, R=2)) % 256 == 0
 

@@ -81,6 +81,11 @@ EDGE = {
     "H8": W.Workload("H8", T=64, H=8, E=8, k=2, R=2, C=64, seed=11),
     "H65536": W.Workload("H65536", T=3, H=65536, E=4, k=2, R=2, C=4, seed=12),
     "H128_fp8": W.Workload("H128", T=64, H=128, E=16, k=4, R=4, C=64, dtype=1, seed=13),
+    # the two-level scan of tile counts: 65 tiles at E = 1024 (just above the
+    # switch), and 102 tiles (a ragged last chunk) at E = 500 (not a multiple
+    # of 32; two thread groups in the chunk scan)
+    "T2049_E1024_chunked": W.Workload("t2049", T=2049, H=64, E=1024, k=6, R=8, C=64, seed=17),
+    "T3239_E500_chunked": W.Workload("t3239", T=3239, H=64, E=500, k=5, R=4, C=100, seed=18),
     # large token counts and capacities: 131072 route tiles; one expert with a million slots
     "T4M": W.Workload("T4M", T=1 << 22, H=8, E=8, k=2, R=2, C=1 << 21, seed=14),
     "E1_C1M": W.Workload("E1_C1M", T=1 << 20, H=8, E=1, k=1, R=1, C=1 << 20, seed=15),
