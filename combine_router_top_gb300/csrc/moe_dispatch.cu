@@ -309,7 +309,7 @@ dispatch_bf16_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restri
 // per destination. Block 0 forms
 // counts, offsets, rank_counts and dropped from the tile counts.
 constexpr int kFusedMaxTiles = 32;             // decode-sized batches: at most 1024 tokens
-constexpr int kFusedThreads = 128;
+constexpr int kFusedThreads = 256;             // two quantise passes at H 7168; 128, 384 and 512 measured no faster
 constexpr int kFusedMaxHidden = 16384;         // staged bf16 row: 2 * H bytes of shared memory
 
 constexpr size_t fused_smem_bytes(int H, int E) {
