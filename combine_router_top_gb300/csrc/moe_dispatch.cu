@@ -241,14 +241,16 @@ dispatch_fp8_seg_kernel(const uint16_t *__restrict__ x, const int32_t *__restric
         if ((tid & 7) == 0) ss[tid >> 3] = sc;
         __syncthreads();
         // every thread stores its 16 codes to each kept destination (the CTA
-        // writes each destination's 1 KB in one coalesced pass), and thread
-        // 8j + b the scale of block b to destination j
+        // writes each destination's segment of codes in one coalesced pass),
+        // and thread kSegBlocks*j + b the scale of block b to destination j
         const int nd = s_n;
         const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
         for (int j = 0; j < nd; ++j)
             st_v4(recv_q + (size_t)s_row[j] * H + (size_t)seg * kFp8Seg + (size_t)tid * 16, qv);
-        for (int i = tid; i < nd * (kFp8Seg / 128); i += kFp8SegThreads)
-            recv_scale[(size_t)s_row[i >> 3] * nb + (size_t)seg * (kFp8Seg / 128) + (i & 7)] = ss[i & 7];
+        constexpr int kSegBlocks = kFp8Seg / 128;            // scales per segment
+        for (int i = tid; i < nd * kSegBlocks; i += kFp8SegThreads)
+            recv_scale[(size_t)s_row[i / kSegBlocks] * nb + (size_t)seg * kSegBlocks + (i % kSegBlocks)] =
+                ss[i % kSegBlocks];
         __syncthreads();                     // ss and s_row are rewritten by the next unit
     }
 }
