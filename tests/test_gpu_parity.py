@@ -80,6 +80,7 @@ EDGE = {
     # hidden extremes
     "H8": W.Workload("H8", T=64, H=8, E=8, k=2, R=2, C=64, seed=11),
     "H65536": W.Workload("H65536", T=3, H=65536, E=4, k=2, R=2, C=4, seed=12),
+    "H65536_fp8": W.Workload("H65536f", T=5, H=65536, E=4, k=2, R=2, C=4, dtype=1, seed=19),
     "H128_fp8": W.Workload("H128", T=64, H=128, E=16, k=4, R=4, C=64, dtype=1, seed=13),
     # the two-level scan of tile counts: 65 tiles at E = 1024 (just above the
     # switch), and 102 tiles (a ragged last chunk) at E = 500 (not a multiple
