@@ -36,24 +36,44 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;                         // rows of one expert per tile
+constexpr int kBM = 128;                         // rows of one MMA (and of one TMA load of A)
 constexpr int kBN = 256;                         // outputs per tile (128 or 256)
 constexpr int kBK = 128;                         // bytes of input per row and block: 128 e4m3 (one scale) or 64 bf16
 constexpr int kNumAcc = 512 / kBN;               // fp32 accumulators that fill the 512 TMEM columns
-constexpr int kGemmStages = (196 * 1024) / (kBM * kBK + kBN * kBK);
 constexpr int kGemmEpiWarps = 16;
 constexpr int kGemmThreads = 32 * (2 + kGemmEpiWarps + 2);   // + 2 idle warps: 20 warps, 96 registers each
 constexpr uint32_t kATileBytes = kBM * kBK;      // 16 KB
 constexpr uint32_t kBTileBytes = kBN * kBK;      // 32 KB
-constexpr uint32_t kGemmStageBytes = kATileBytes + kBTileBytes;
 constexpr uint32_t kGemmTmemCols = kNumAcc * kBN;   // all 512 columns
 constexpr int kEpiCols = kBN / 4;                // columns per promotion warp (4 per TMEM lane quadrant)
-constexpr size_t kGemmSmemBytes = kGemmStages * kGemmStageBytes + 1024;   // + alignment slack
+
+// Tile geometry. Tiles of 128 rows (one MMA row block): stages of A 16 KB +
+// B 32 KB, four of them. WIDE (bf16 only): tiles of up to 256 rows, two
+// 128-row MMAs sharing each B tile, so a third fewer operand bytes per FLOP
+// and each weight tile read once per pair of row blocks; stages of A 32 KB +
+// B 32 KB, three of them. Chosen on the host for experts that average 512
+// rows or more; with about 256 rows per expert the narrow tiles are faster
+// (the wide tile's epilogue cannot overlap the next tile, since its two
+// halves fill TMEM, and its ragged one-half remainders lose the fourth stage).
+template <bool WIDE>
+struct GemmGeom {
+    static constexpr int kTileRows = WIDE ? 2 * kBM : kBM;
+    static constexpr uint32_t kARegion = (uint32_t)kTileRows * kBK;
+    static constexpr uint32_t kStageBytes = kARegion + kBTileBytes;
+    static constexpr int kStages = (196 * 1024) / kStageBytes;
+};
+constexpr size_t kGemmSmemBytes =
+    (GemmGeom<false>::kStages * GemmGeom<false>::kStageBytes > GemmGeom<true>::kStages * GemmGeom<true>::kStageBytes
+         ? GemmGeom<false>::kStages * GemmGeom<false>::kStageBytes
+         : GemmGeom<true>::kStages * GemmGeom<true>::kStageBytes) +
+    1024;                                        // + alignment slack
+constexpr int kWideMinRows = 512;               // mean kept rows per expert from which bf16 takes wide tiles
 constexpr unsigned kGemmPollLimit = 1u << 20;
 
 // Shared-memory matrix descriptor of a K-major tile whose rows are 128 bytes,
@@ -137,7 +157,7 @@ __device__ __forceinline__ bool gemm_wait(uint32_t bar, uint32_t parity, volatil
 // s_first[e] = index of expert e's first tile, s_first[E] = the total.
 struct TileList {
     const int *first, *kept;
-    int E, n_tiles;
+    int E, n_tiles, tile_rows;
     __device__ __forceinline__ void decode(int t, int &e, int &nt, int &mt, int &rows) const {
         int lo = 0, hi = E;                          // first[lo] <= t < first[hi]
         while (hi - lo > 1) {
@@ -149,21 +169,24 @@ struct TileList {
         const int local = t - first[e];
         nt = local / mtiles;
         mt = local - nt * mtiles;
-        rows = min(kept[e] - mt * kBM, kBM);
+        rows = min(kept[e] - mt * tile_rows, tile_rows);
     }
 };
 
 // FP8: per-block promotion (fresh accumulator per block of 128 inputs, scaled
 // in registers). BF16: no scales, so one accumulator holds a whole tile and
 // the promotion warps only convert and store it.
-template <bool FP8>
+template <bool FP8, bool WIDE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                        const float *__restrict__ a_scale, const int32_t *__restrict__ counts,
                        const float *__restrict__ w_scale, uint16_t *__restrict__ y, int H, int C, int E,
                        unsigned *status) {
+    static_assert(!(FP8 && WIDE), "wide tiles are for bf16 rows");
+    constexpr int kStages = GemmGeom<WIDE>::kStages, TR = GemmGeom<WIDE>::kTileRows;
+    constexpr uint32_t kStageBytes = GemmGeom<WIDE>::kStageBytes, kARegion = GemmGeom<WIDE>::kARegion;
     extern __shared__ uint8_t gemm_smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kGemmStages], empty_bar[kGemmStages];
+    __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
     __shared__ __align__(8) uint64_t tfull_bar[kNumAcc], tempty_bar[kNumAcc];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -177,7 +200,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     const uint32_t smem0 = (smem_u32(gemm_smem_raw) + 1023u) & ~1023u;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kGemmStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
@@ -195,7 +218,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         for (int e = lane * per; e < min(E, lane * per + per); ++e) {
             const int kept = min(__ldg(counts + e), C);
             s_kept[e] = kept;
-            sum += (kept + kBM - 1) / kBM * n_tiles;
+            sum += (kept + TR - 1) / TR * n_tiles;
         }
         int incl = sum;
 #pragma unroll
@@ -206,7 +229,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         int run = incl - sum;
         for (int e = lane * per; e < min(E, lane * per + per); ++e) {
             s_first[e] = run;
-            run += (s_kept[e] + kBM - 1) / kBM * n_tiles;
+            run += (s_kept[e] + TR - 1) / TR * n_tiles;
         }
         if (lane == 31) s_first[E] = incl;
     }
@@ -216,7 +239,7 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         pdl_launch_dependents();
         return;
     }
-    const TileList tiles{s_first, s_kept, E, n_tiles};
+    const TileList tiles{s_first, s_kept, E, n_tiles, TR};
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                      "r"(kGemmTmemCols)
@@ -229,23 +252,26 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     const uint32_t tmem = s_tmem;
 
     uint32_t issued = 0;                          // producer: stages loaded
-    uint32_t committed = 0;                       // MMA issuer: accumulators committed
+    uint32_t last_tfull = 0, last_tfull_par = 0;  // MMA issuer: the last accumulator commit
+    bool committed = false;
     if (warp == 0) {
         if (lane == 0) {
             uint32_t g = 0;
             for (int t = blockIdx.x; t < total && !s_abort; t += gridDim.x) {
                 int e, nt, mt, rows;
                 tiles.decode(t, e, nt, mt, rows);
-                const int row_a = e * C + mt * kBM;
+                const int row_a = e * C + mt * TR;
                 const int row_b = e * H + nt * kBN;
+                const int a_boxes = rows > kBM ? 2 : 1;      // 128-row A loads this tile needs
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
-                    const int s = g % kGemmStages;
-                    if (g >= kGemmStages &&
-                        !gemm_wait(smem_u32(&empty_bar[s]), ((g / kGemmStages) + 1) & 1, &s_abort))
+                    const int s = g % kStages;
+                    if (g >= kStages && !gemm_wait(smem_u32(&empty_bar[s]), ((g / kStages) + 1) & 1, &s_abort))
                         break;
-                    const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kATileBytes;
-                    mbar_expect_tx(&full_bar[s], kGemmStageBytes);
-                    tma_load_2d(sa, &map_a, smem_u32(&full_bar[s]), kb * kb_elems, row_a);
+                    const uint32_t sa = smem0 + s * kStageBytes, sb = sa + kARegion;
+                    mbar_expect_tx(&full_bar[s], a_boxes * kATileBytes + kBTileBytes);
+                    for (int h = 0; h < a_boxes; ++h)
+                        tma_load_2d(sa + h * kATileBytes, &map_a, smem_u32(&full_bar[s]), kb * kb_elems,
+                                    row_a + h * kBM);
                     tma_load_2d(sb, &map_b, smem_u32(&full_bar[s]), kb * kb_elems, row_b);
                     issued = g + 1;
                 }
@@ -254,29 +280,93 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     } else if (warp == 1) {
         if (lane == 0) {
             uint32_t g = 0;                       // blocks consumed (stage ring)
-            uint32_t a = 0;                       // accumulators used (FP8: per block, BF16: per tile)
+            uint32_t a = 0;                       // accumulators used: FP8 one per block, BF16 one per tile
+            uint32_t uses[kNumAcc] = {};          // WIDE: commits of each TMEM half (accumulator)
+            int next_h = 0;                       // WIDE: the half a one-half tile takes next
             bool stop = false;
             for (int t = blockIdx.x; t < total && !stop && !s_abort; t += gridDim.x) {
+                // WIDE: the tile takes halves h0 .. h0 + halves - 1 (one per 128 rows);
+                // one-half tiles alternate, as the issuer and the epilogue both count
+                int halves = 1, h0 = 0;
+                if constexpr (WIDE) {
+                    int e, nt, mt, rows;
+                    tiles.decode(t, e, nt, mt, rows);
+                    halves = rows > kBM ? 2 : 1;
+                    h0 = halves == 2 ? 0 : next_h;
+                    next_h = halves == 2 ? 0 : 1 - h0;
+                }
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
-                    const int s = g % kGemmStages;
-                    const int buf = a % kNumAcc;
-                    if (!gemm_wait(smem_u32(&full_bar[s]), (g / kGemmStages) & 1, &s_abort)) { stop = true; break; }
-                    if ((FP8 || kb == 0) && a >= kNumAcc &&
-                        !gemm_wait(smem_u32(&tempty_bar[buf]), ((a / kNumAcc) + 1) & 1, &s_abort)) {
-                        stop = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = smem0 + s * kGemmStageBytes, sb = sa + kATileBytes;
-                    const uint32_t d = tmem + buf * kBN;
+                    const int s = g % kStages;
+                    if (!gemm_wait(smem_u32(&full_bar[s]), (g / kStages) & 1, &s_abort)) { stop = true; break; }
+                    const uint32_t sa = smem0 + s * kStageBytes, sb = sa + kARegion;
+                    if constexpr (FP8) {
+                        const int buf = a % kNumAcc;
+                        if (a >= kNumAcc &&
+                            !gemm_wait(smem_u32(&tempty_bar[buf]), ((a / kNumAcc) + 1) & 1, &s_abort)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem + buf * kBN;
 #pragma unroll
-                    for (int k = 0; k < kBK / 32; ++k)
-                        mma_k32b<FP8>(d, umma_desc_sw128(sa + 32 * k), umma_desc_sw128(sb + 32 * k),
-                                      (k > 0 || (!FP8 && kb > 0)) ? 1u : 0u);
-                    mma_commit(smem_u32(&empty_bar[s]));
-                    if (FP8 || kb == nkb - 1) {
+                        for (int k = 0; k < kBK / 32; ++k)
+                            mma_k32b<FP8>(d, umma_desc_sw128(sa + 32 * k), umma_desc_sw128(sb + 32 * k),
+                                          k > 0 ? 1u : 0u);
+                        mma_commit(smem_u32(&empty_bar[s]));
                         mma_commit(smem_u32(&tfull_bar[buf]));
-                        committed = ++a;
+                        last_tfull = smem_u32(&tfull_bar[buf]);
+                        last_tfull_par = (a / kNumAcc) & 1;
+                        committed = true;
+                        ++a;
+                    } else if constexpr (!WIDE) {
+                        // one accumulator per tile, alternating (a counts tiles)
+                        const int buf = a % kNumAcc;
+                        if (kb == 0 && a >= kNumAcc &&
+                            !gemm_wait(smem_u32(&tempty_bar[buf]), ((a / kNumAcc) + 1) & 1, &s_abort)) {
+                            stop = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem + buf * kBN;
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k)
+                            mma_k32b<FP8>(d, umma_desc_sw128(sa + 32 * k), umma_desc_sw128(sb + 32 * k),
+                                          (k > 0 || kb > 0) ? 1u : 0u);
+                        mma_commit(smem_u32(&empty_bar[s]));
+                        if (kb == nkb - 1) {
+                            mma_commit(smem_u32(&tfull_bar[buf]));
+                            last_tfull = smem_u32(&tfull_bar[buf]);
+                            last_tfull_par = (a / kNumAcc) & 1;
+                            committed = true;
+                            ++a;
+                        }
+                    } else {
+                        if (kb == 0) {            // the halves' previous tiles must have been read
+                            for (int hh = 0; hh < halves && !stop; ++hh) {
+                                const int h = h0 + hh;
+                                if (uses[h] > 0 &&
+                                    !gemm_wait(smem_u32(&tempty_bar[h]), (uses[h] - 1) & 1, &s_abort))
+                                    stop = true;
+                            }
+                            if (stop) break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < kBK / 32; ++k)
+                            for (int hh = 0; hh < halves; ++hh)
+                                mma_k32b<FP8>(tmem + (h0 + hh) * kBN, umma_desc_sw128(sa + hh * kATileBytes + 32 * k),
+                                              umma_desc_sw128(sb + 32 * k), (k > 0 || kb > 0) ? 1u : 0u);
+                        mma_commit(smem_u32(&empty_bar[s]));
+                        if (kb == nkb - 1) {
+                            for (int hh = 0; hh < halves; ++hh) {
+                                const int h = h0 + hh;
+                                mma_commit(smem_u32(&tfull_bar[h]));
+                                last_tfull = smem_u32(&tfull_bar[h]);
+                                last_tfull_par = uses[h] & 1;
+                                ++uses[h];
+                            }
+                            committed = true;
+                        }
                     }
                 }
             }
@@ -284,8 +374,10 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     } else if (warp < 2 + kGemmEpiWarps) {
         const int quad = warp & 3;                        // TMEM lanes this warp may read
         const int cg = (warp - 2) >> 2;                   // which quarter of the tile's columns
-        const int r = quad * 32 + lane;                   // row within the tile
+        const int r = quad * 32 + lane;                   // row within a 128-row block of the tile
         uint32_t g = 0;
+        uint32_t uses[kNumAcc] = {};                      // WIDE: reads of each TMEM half, as the issuer counts
+        int next_h = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             int e, nt, mt, rows;
@@ -293,8 +385,8 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             const int col0 = nt * kBN + cg * kEpiCols;         // this warp's first output column
             const int nblk = col0 / 128;                       // its 128-output weight-scale block
             const bool live = r < rows && col0 < H;
-            const size_t grow = (size_t)e * C + (size_t)mt * kBM + r;
-            if constexpr (!FP8) {
+            const size_t grow = (size_t)e * C + (size_t)mt * TR + r;
+            if constexpr (!FP8 && !WIDE) {
                 // the tile's whole sum is in one accumulator: convert and store
                 const int buf = g % kNumAcc;
                 int got = 0;
@@ -313,18 +405,58 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     tmem_ld_wait();
                     if (live) {
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            dst[2 * c + h] = make_uint4(
-                                pack_bf16x2(__uint_as_float(v[8 * h + 0]), __uint_as_float(v[8 * h + 1])),
-                                pack_bf16x2(__uint_as_float(v[8 * h + 2]), __uint_as_float(v[8 * h + 3])),
-                                pack_bf16x2(__uint_as_float(v[8 * h + 4]), __uint_as_float(v[8 * h + 5])),
-                                pack_bf16x2(__uint_as_float(v[8 * h + 6]), __uint_as_float(v[8 * h + 7])));
+                        for (int q = 0; q < 2; ++q)
+                            dst[2 * c + q] = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty_bar[buf]);
                 ++g;
+                continue;
+            }
+            if constexpr (WIDE) {
+                // the tile's whole sum is in one TMEM half per 128 rows: convert and store
+                const int halves = rows > kBM ? 2 : 1;
+                const int h0 = halves == 2 ? 0 : next_h;
+                next_h = halves == 2 ? 0 : 1 - h0;
+                for (int hh = 0; hh < halves; ++hh) {
+                    const int h = h0 + hh;
+                    int got = 0;
+                    if (lane == 0) got = gemm_wait(smem_u32(&tfull_bar[h]), uses[h] & 1, &s_abort) ? 1 : 0;
+                    if (!__shfl_sync(kFull, got, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const bool live_h = hh * kBM + r < rows && col0 < H;
+                    const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + h * kBN + cg * kEpiCols;
+                    uint4 *dst = reinterpret_cast<uint4 *>(y + (grow + (size_t)hh * kBM) * H + (size_t)nt * kBN +
+                                                           cg * kEpiCols);
+#pragma unroll
+                    for (int c = 0; c < kEpiCols / 16; ++c) {
+                        uint32_t v[16];
+                        tmem_ld16(taddr + 16 * c, v);
+                        tmem_ld_wait();
+                        if (live_h) {
+#pragma unroll
+                            for (int q = 0; q < 2; ++q)
+                                dst[2 * c + q] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty_bar[h]);
+                    ++uses[h];
+                }
                 continue;
             }
             const float *sa_row = a_scale + grow * nb;
@@ -377,11 +509,11 @@ expert_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         volatile int no_abort = 0;
         if (warp == 0 && lane == 0) {
             atomicOr(status, kStatusWaitGaveUp);
-            for (uint32_t g = (issued > kGemmStages ? issued - kGemmStages : 0); g < issued; ++g)
-                gemm_wait(smem_u32(&full_bar[g % kGemmStages]), (g / kGemmStages) & 1, &no_abort);
+            for (uint32_t g = (issued > kStages ? issued - kStages : 0); g < issued; ++g)
+                gemm_wait(smem_u32(&full_bar[g % kStages]), (g / kStages) & 1, &no_abort);
         }
-        if (warp == 1 && lane == 0 && committed > 0)
-            gemm_wait(smem_u32(&tfull_bar[(committed - 1) % kNumAcc]), ((committed - 1) / kNumAcc) & 1, &no_abort);
+        if (warp == 1 && lane == 0 && committed)   // the last commit: every MMA before it is complete with it
+            gemm_wait(last_tfull, last_tfull_par, &no_abort);
         __syncthreads();
     }
     if (warp == 1) {
@@ -423,7 +555,7 @@ bool encode_tile_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool FP8>
+template <bool FP8, bool WIDE>
 int launch_gemm(const Dims &d, const void *recv, const float *recv_scale, const int32_t *counts, const void *w,
                 const float *w_scale, void *y, void *stream) {
     const int eb = FP8 ? 1 : 2;
@@ -437,14 +569,14 @@ int launch_gemm(const Dims &d, const void *recv, const float *recv_scale, const 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
     if (!smem_set[dev]) {
-        if (cudaFuncSetAttribute(expert_gemm_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(expert_gemm_kernel<FP8, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kGemmSmemBytes) != cudaSuccess)
             return MOE_ERR_CUDA;
         smem_set[dev] = true;
     }
     int grid = sm_count();                        // persistent: one CTA per SM
     if (d.max_blocks > 0 && d.max_blocks < grid) grid = d.max_blocks;
-    if (launch_pdl_smem(expert_gemm_kernel<FP8>, grid, kGemmThreads, kGemmSmemBytes, as_stream(stream), map_a,
+    if (launch_pdl_smem(expert_gemm_kernel<FP8, WIDE>, grid, kGemmThreads, kGemmSmemBytes, as_stream(stream), map_a,
                         map_b, recv_scale, counts, w_scale, static_cast<uint16_t *>(y), d.H, d.C, d.E, status) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
@@ -466,7 +598,7 @@ extern "C" int moe_expert_gemm_fp8(const moe_problem *p, const void *recv_q, con
     if (!aligned(recv_q, 16) || !aligned(w_q, 16) || !aligned(y, 16) || !aligned(recv_scale, 4) ||
         !aligned(w_scale, 4) || !aligned(counts, 4))
         return MOE_ERR_INVALID_ARG;
-    return launch_gemm<true>(d, recv_q, recv_scale, counts, w_q, w_scale, y, stream);
+    return launch_gemm<true, false>(d, recv_q, recv_scale, counts, w_q, w_scale, y, stream);
 }
 
 extern "C" int moe_expert_gemm_bf16(const moe_problem *p, const void *recv_x, const int32_t *counts,
@@ -479,5 +611,9 @@ extern "C" int moe_expert_gemm_bf16(const moe_problem *p, const void *recv_x, co
     if (!recv_x || !counts || !w || !y) return MOE_ERR_INVALID_ARG;
     if (!aligned(recv_x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(counts, 4))
         return MOE_ERR_INVALID_ARG;
-    return launch_gemm<false>(d, recv_x, nullptr, counts, w, nullptr, y, stream);
+    // wide tiles when the experts average kWideMinRows kept rows or more
+    // (counts are on the device: the mean follows from the problem's sizes)
+    const long long mean_rows = std::min<long long>((long long)d.T * d.k / d.E, (long long)d.C);
+    if (mean_rows >= kWideMinRows) return launch_gemm<false, true>(d, recv_x, nullptr, counts, w, nullptr, y, stream);
+    return launch_gemm<false, false>(d, recv_x, nullptr, counts, w, nullptr, y, stream);
 }

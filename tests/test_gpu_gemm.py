@@ -206,6 +206,9 @@ CASES_BF16 = {
     "H512_two_row_tiles": (W.Workload("b512", T=150, H=512, E=2, k=2, R=1, C=160, seed=303), None),
     "H2048": (W.Workload("b2048", T=24, H=2048, E=2, k=2, R=2, C=32, seed=304), None),
     "overflow_and_empty": (W.Workload("bov", T=64, H=256, E=8, k=2, R=4, C=8, seed=305), [2, 5]),
+    # 600 rows per expert on average: the host picks 256-row tiles (two TMEM
+    # halves per tile, 256 + 256 + a one-half remainder of 88 rows)
+    "H256_wide_600": (W.Workload("b600", T=600, H=256, E=2, k=2, R=1, C=640, seed=307), None),
     # about 300 rows per expert: three 128-row tiles, the last one ragged
     "H256_three_row_blocks": (W.Workload("b300", T=300, H=256, E=2, k=2, R=1, C=320, seed=306), None),
 }
@@ -246,14 +249,16 @@ def test_gemm_bf16_matches_oracle(case, max_blocks):
     print(f"bf16 {case} max_blocks={max_blocks}: max |err| / S = {worst:.3g}")
 
 
-@pytest.mark.parametrize("name", ["v2lite", "dbo_prefill"])
+@pytest.mark.parametrize("name", ["v2lite", "dbo_prefill", "prefill_32_wide"])
 def test_gemm_bf16_full_size_sampled_rows(name):
-    """DeepSeek-V2-Lite decode (256 tokens, H 2048, 64 experts) and the 8192-token
+    """DeepSeek-V2-Lite decode (256 tokens, H 2048, 64 experts), the 8192-token
     dual-batch prefill shape (H 7168, 256 experts, C 1024; 26 GB of device-drawn
-    weights): route -> dispatch -> GEMM on the GPU, sampled rows against the
-    oracle fed by its own dispatch."""
+    weights) and the same prefill over 32 experts (1024 kept rows each: the
+    256-row tiles): route -> dispatch -> GEMM on the GPU, sampled rows against
+    the oracle fed by its own dispatch."""
     import combine_router_top_gb300 as M
-    w = W.WORKLOADS["v2lite"] if name == "v2lite" else W.WORKLOADS["dbo"]
+    w = {"v2lite": W.WORKLOADS["v2lite"], "dbo_prefill": W.WORKLOADS["dbo"],
+         "prefill_32_wide": W.WORKLOADS["dbo"].with_(E=32)}[name]
     rx, counts = oracle_dispatch_bf16(w)
     p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, M.MOE_DTYPE_BF16)
     b = M.alloc_buffers(p, DEV)
@@ -271,7 +276,8 @@ def test_gemm_bf16_full_size_sampled_rows(name):
     kept = np.minimum(counts, w.C)
     live = [e for e in range(w.E) if kept[e] > 0]
     emax = int(np.argmax(kept))
-    picks = [(live[0], 0), (live[-1], kept[live[-1]] - 1), (emax, kept[emax] - 1), (emax, min(130, kept[emax] - 1))]
+    picks = [(live[0], 0), (live[-1], kept[live[-1]] - 1), (emax, kept[emax] - 1), (emax, min(130, kept[emax] - 1)),
+             (emax, min(255, kept[emax] - 1)), (emax, min(256, kept[emax] - 1)), (emax, min(383, kept[emax] - 1))]
     worst = 0.0
     for e, r in picks:
         yr = y[e, r].cpu().numpy().view(np.uint16)
