@@ -845,11 +845,14 @@ def run_gemm(args, dev, reps: int = 10, experts: int = 0) -> dict:
     del wq, ws
     torch.cuda.empty_cache()
 
-    # bf16 rows, bf16 weights (tcgen05 kind::f16): DeepSeek-V2-Lite decode and
-    # the 8192-token prefill shape (26 GB of weights at H 7168, 256 experts);
+    # bf16 rows, bf16 weights (tcgen05 kind::f16): DeepSeek-V2-Lite decode, the
+    # 8192-token prefill shape (26 GB of weights at H 7168, 256 experts) and the
+    # skewed Mixtral-shaped prefill (8 experts, about 1024 rows each on average:
+    # the 256-row tiles; 268 MB of weights and 67 MB of rows, more than L2);
     # the bound is whichever of HBM and the bf16 tensor peak takes longer
     bf16_burst, bf16_sust = fp8_burst / FP8_PER_BF16, fp8_sust / FP8_PER_BF16
-    cases = [("decode_bf16", W.WORKLOADS["v2lite"]), ("prefill_bf16", W.WORKLOADS["dbo"])]
+    cases = [("decode_bf16", W.WORKLOADS["v2lite"]), ("prefill_bf16", W.WORKLOADS["dbo"]),
+             ("prefill_bf16_mixtral", W.WORKLOADS["mixtral_skew"])]
     if experts:
         cases = [(n, w.with_(E=experts, R=min(w.R, experts))) for n, w in cases]
     for name, w in cases:
