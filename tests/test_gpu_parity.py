@@ -377,6 +377,34 @@ def test_dbo_small_and_odd_batches(T):
 
 
 
+def test_dbo_step_fp8_dispatch():
+    """The dual-batch step with fp8 dispatch (DeepSeek-V3 shape, two micro-batches
+    of 256 tokens): output within 1 ulp of the oracle's, each micro-batch's codes
+    and scales bit-exact."""
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev, to_host, ulp_distance, valid_rows
+    w = W.WORKLOADS["dsv3_fp8"].with_(T=512)
+    x, lg, s = W.make_x(w), W.make_logits(w), W.expert_scale(w)
+    dt = M.MOE_DTYPE_FP8_E4M3_B128
+    pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, dt)
+    bufs = [M.alloc_buffers(M.problem(w.T // 2, w.H, w.E, w.k, w.R, w.C, dt), "cuda:0") for _ in range(2)]
+    out = torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0")
+    comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    ctx = M.dbo_create()
+    comp.wait_stream(torch.cuda.current_stream())
+    M.dbo_step(ctx, pf, to_dev(x), to_dev(lg), to_dev(s), bufs, out, comp, comm)
+    torch.cuda.synchronize()
+    o = O.run_dbo(x, lg, s, w.k, w.R, w.C, True)
+    assert ulp_distance(to_host(out, np.uint16), o["out"]).max() <= 1
+    for u in range(2):
+        ref = o["parts"][u]
+        e, r = valid_rows(ref["counts"], w.C)
+        assert np.array_equal(to_host(bufs[u]["recv"])[e, r], ref["recv_q"][e, r])
+        assert np.array_equal(to_host(bufs[u]["recv_scale"])[e, r].view(np.uint32), ref["recv_scale"][e, r].view(np.uint32))
+    ctx.close()
+
+
 def _layers_setup(w, L, alpha, sigma, busy=0):
     import torch
     import combine_router_top_gb300 as M
