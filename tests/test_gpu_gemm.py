@@ -73,7 +73,7 @@ def oracle_dispatch(w: W.Workload):
     return rq, rs, c["counts"]
 
 
-def run_gemm(w: W.Workload, rq, rs, counts, wq, ws):
+def run_gemm(w: W.Workload, rq, rs, counts, wq, ws, max_blocks=0):
     import combine_router_top_gb300 as M
     E, C, H = rq.shape
     rng = np.random.default_rng(w.seed)
@@ -83,7 +83,7 @@ def run_gemm(w: W.Workload, rq, rs, counts, wq, ws):
         kept = min(int(counts[e]), C)
         rq_dev[e, kept:] = rng.integers(0, 256, size=(C - kept, H), dtype=np.uint8)
         rs_dev[e, kept:] = np.nan
-    p = M.problem(w.T, H, E, w.k, w.R, C, M.MOE_DTYPE_FP8_E4M3_B128)
+    p = M.problem(w.T, H, E, w.k, w.R, C, M.MOE_DTYPE_FP8_E4M3_B128, max_blocks)
     y = torch.full((E, C, H), SENTINEL, dtype=torch.int32, device=DEV).to(torch.int16)
     M.moe_expert_gemm_fp8(p, torch.from_numpy(rq_dev).to(DEV), torch.from_numpy(rs_dev).to(DEV),
                           torch.from_numpy(np.ascontiguousarray(counts, dtype=np.int32)).to(DEV),
@@ -107,8 +107,11 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("max_blocks", [0, 1, 3])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_gemm_matches_oracle(case):
+def test_gemm_matches_oracle(case, max_blocks):
+    """Small grids (one CTA, three CTAs) walk many tiles per CTA, so the two
+    TMEM accumulators alternate across blocks and tiles within one CTA."""
     w, empty = CASES[case]
     rq, rs, counts = oracle_dispatch(w)
     counts = counts.copy()
@@ -116,14 +119,14 @@ def test_gemm_matches_oracle(case):
         counts[empty] = 0
     wq, ws = W.make_weights(w)
     y_ref = O.expert_gemm_fp8(rq, rs, counts, wq, ws)
-    y = run_gemm(w, rq, rs, counts, wq, ws)
+    y = run_gemm(w, rq, rs, counts, wq, ws, max_blocks)
     worst = 0.0
     for e in range(w.E):
         kept = min(int(counts[e]), w.C)
         assert np.all(y[e, kept:] == SENTINEL), f"expert {e}: rows past the count were written"
         for r in range(kept):
             worst = max(worst, check_row(y[e, r], y_ref[e, r], abs_bound_row(rq[e, r], rs[e, r], wq[e], ws[e])))
-    print(f"{case}: max |err| / S = {worst:.3g}")
+    print(f"{case} max_blocks={max_blocks}: max |err| / S = {worst:.3g}")
 
 
 @pytest.mark.parametrize("name", ["dsv3_decode", "dsv3_prefill"])
