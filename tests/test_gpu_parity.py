@@ -405,6 +405,56 @@ def test_dbo_step_fp8_dispatch():
     ctx.close()
 
 
+def test_repeated_runs_are_bit_identical():
+    """The paths whose kernels run concurrently or signal one another, repeated:
+    the PDL-chained step (separate and fused route + dispatch, alternately), the
+    readiness kernel with a new epoch each time, and the two-stream dual-batch
+    step; every run equals the first bit for bit."""
+    import torch
+    import combine_router_top_gb300 as M
+    w = W.WORKLOADS["dsv3_fp8"]
+    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
+    b = M.alloc_buffers(p, "cuda:0")
+    x = torch.from_numpy(W.make_x(w).view(np.int16)).to("cuda:0")
+    lg = torch.from_numpy(W.make_logits(w)).to("cuda:0")
+    s = torch.from_numpy(W.expert_scale(w)).to("cuda:0")
+    out = torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0")
+    M.run_path(p, x, lg, s, b, out)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    for i in range(200):
+        out.zero_()
+        M.run_path(p, x, lg, s, b, out, fused=(i % 2 == 1))
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"step, run {i}"
+        out.zero_()
+        M.moe_expert_combine(p, b["recv"], b["recv_scale"], b["counts"], s, b["y"], b["topk_idx"], b["topk_w"],
+                             b["slot"], out, b["ready_flags"], i + 1)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"readiness kernel, run {i}"
+    assert M.moe_device_status() == M.MOE_OK
+    w = W.WORKLOADS["v2lite"].with_(T=2048)
+    pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C)
+    x = torch.from_numpy(W.make_x(w).view(np.int16)).to("cuda:0")
+    lg = torch.from_numpy(W.make_logits(w)).to("cuda:0")
+    s = torch.from_numpy(W.expert_scale(w)).to("cuda:0")
+    bufs = [M.alloc_buffers(M.problem(w.T // 2, w.H, w.E, w.k, w.R, w.C), "cuda:0") for _ in range(2)]
+    out = torch.empty((w.T, w.H), dtype=torch.int16, device="cuda:0")
+    comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    ctx = M.dbo_create()
+    comp.wait_stream(torch.cuda.current_stream())
+    M.dbo_step(ctx, pf, x, lg, s, bufs, out, comp, comm)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    for i in range(200):
+        out.zero_()
+        torch.cuda.synchronize()
+        M.dbo_step(ctx, pf, x, lg, s, bufs, out, comp, comm)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"dual-batch step, run {i}"
+    ctx.close()
+
+
 def _layers_setup(w, L, alpha, sigma, busy=0):
     import torch
     import combine_router_top_gb300 as M
