@@ -624,3 +624,38 @@ def test_layer_stand_in_is_exact():
         M.moe_layer_stand_in(to_dev(x), out, a, busy)
         torch.cuda.synchronize()
         assert np.array_equal(to_host(out, np.uint16), O.scale_rows(x, a))
+
+
+def test_fp32_order_cases_by_hand():
+    """The hand-derived cases that fix combine's fp32 accumulation (fused multiply-adds in ascending j
+    from +0) and the fp8 stand-in's product order ((q * scale) * s_e): the kernels give the derived
+    bits, where any other order would not."""
+    import json
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev, to_host
+    with open(os.path.join(os.path.dirname(__file__), "golden", "combine_fp32_order.json")) as fh:
+        g = json.load(fh)
+    H = 8
+    for c in g["combine"]:
+        k = c["k"]
+        p = M.problem(1, H, k, k, 1, 1, M.MOE_DTYPE_BF16)
+        y = np.repeat(np.array([int(h, 16) for h in c["y_bf16_bits"]], np.uint16).reshape(k, 1, 1), H, axis=2)
+        w = np.array([[int(h, 16) for h in c["w_f32_bits"]]], np.uint32).view(np.float32)
+        out = torch.full((1, H), 0x7777, dtype=torch.int16, device="cuda:0")
+        M.moe_combine(p, to_dev(y), to_dev(np.arange(k, dtype=np.int32).reshape(1, k)), to_dev(w),
+                      to_dev(np.zeros((1, k), np.int32)), out)
+        torch.cuda.synchronize()
+        assert np.all(to_host(out, np.uint16) == int(c["out_bf16_bits"], 16)), c["name"]
+    c = g["expert_fp8"][0]
+    Hq = c["H"]
+    p = M.problem(1, Hq, 2, 1, 1, 1, M.MOE_DTYPE_FP8_E4M3_B128)
+    recv = np.zeros((2, 1, Hq), np.uint8)
+    recv[1, 0, :] = int(c["code"], 16)
+    scale = np.array([int(c["scale_f32_bits"], 16)], np.uint32).view(np.float32)[0]
+    s = np.array([1.0, np.array([int(c["s_e_f32_bits"], 16)], np.uint32).view(np.float32)[0]], np.float32)
+    yd = torch.zeros((2, 1, Hq), dtype=torch.int16, device="cuda:0")
+    M.moe_expert_synthetic(p, to_dev(recv), to_dev(np.full((2, 1, Hq // 128), scale, np.float32)),
+                           to_dev(np.array([0, 1], np.int32)), to_dev(s), yd)
+    torch.cuda.synchronize()
+    assert np.all(to_host(yd, np.uint16)[1, 0] == int(c["y_bf16_bits"], 16))

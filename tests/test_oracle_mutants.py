@@ -58,6 +58,29 @@ MUTANTS = {
     # combine: only the first choice summed
     "combine_first_choice_only": ("            for (int32_t j = 0; j < k; ++j) {\n                int32_t s = slot",
                                   "            for (int32_t j = 0; j < 1; ++j) {\n                int32_t s = slot"),
+    # combine: choices summed from the last to the first
+    "combine_descending_j": ("            for (int32_t j = 0; j < k; ++j) {\n                int32_t s = slot",
+                             "            for (int32_t j = k - 1; j >= 0; --j) {\n                int32_t s = slot"),
+    # combine: the product rounded to fp32 before it is added
+    "combine_unfused": ("acc = fmaf(topk_w[(int64_t)t * k + j], bf16_decode(y[row * H + h]), acc);",
+                        "acc = acc + topk_w[(int64_t)t * k + j] * bf16_decode(y[row * H + h]);"),
+    # combine: the accumulator held in double
+    "combine_double_acc": ("            float acc = 0.0f;\n            for (int32_t j = 0; j < k; ++j) {\n"
+                           "                int32_t s = slot[(int64_t)t * k + j];\n                if (s < 0)\n"
+                           "                    continue;\n"
+                           "                int64_t row = (int64_t)topk_idx[(int64_t)t * k + j] * C + s;\n"
+                           "                acc = fmaf(",
+                           "            double acc = 0.0;\n            for (int32_t j = 0; j < k; ++j) {\n"
+                           "                int32_t s = slot[(int64_t)t * k + j];\n                if (s < 0)\n"
+                           "                    continue;\n"
+                           "                int64_t row = (int64_t)topk_idx[(int64_t)t * k + j] * C + s;\n"
+                           "                acc = fma("),
+    # combine: the sum started from -0
+    "combine_starts_negative_zero": ("            float acc = 0.0f;\n            for (int32_t j = 0; j < k; ++j) {",
+                                     "            float acc = -0.0f;\n            for (int32_t j = 0; j < k; ++j) {"),
+    # fp8 expert: the two scales multiplied first
+    "expert_fp8_scale_first": ("float deq = e4m3_decode(((const uint8_t *)recv)[row * H + h]) * recv_scale[row * nb + h / 128];\n                    v = deq * s[e];",
+                               "float deq = e4m3_decode(((const uint8_t *)recv)[row * H + h]) * (recv_scale[row * nb + h / 128] * s[e]);\n                    v = deq;"),
     # gemm: the weight read transposed (w[k][n] instead of w[n][k]), kept in bounds
     "gemm_weight_transposed": ("block += (double)e4m3_decode(q_row[i]) * (double)e4m3_decode(wn[i]);",
                                "block += (double)e4m3_decode(q_row[i]) * (double)e4m3_decode(w[(int64_t)(i % N) * K + n % K]);"),

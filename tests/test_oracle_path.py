@@ -365,6 +365,61 @@ def test_combine_skips_dropped_pairs_without_renormalising():
     assert np.all(bf16_vals(r["out"][gone]) == 0)
 
 
+def _exact(expr: str) -> float:
+    """Value of a golden file's exact expression such as "2033633*2^-29", "1+2^-8" or "257/256"
+    (every one of them is exactly representable in float64)."""
+    return float(eval(expr.replace("^", "**"), {"__builtins__": {}}, {}))
+
+
+def _f32_from_hex(h: str) -> np.float32:
+    return np.array([int(h, 16)], dtype=np.uint32).view(np.float32)[0]
+
+
+def _order_golden():
+    with open(os.path.join(GOLDEN, "combine_fp32_order.json")) as fh:
+        return json.load(fh)
+
+
+@pytest.mark.parametrize("case", [c["name"] for c in _order_golden()["combine"]])
+def test_combine_fp32_ascending_fma_order_by_hand(case):
+    """[PMC §Combine] weighted sum, read as fp32 fused multiply-adds in ascending j from +0 and one
+    bf16 rounding: hand-derived cases on which descending j, an unfused product, a double
+    accumulator or a -0 start each give another bf16 result."""
+    c = next(c for c in _order_golden()["combine"] if c["name"] == case)
+    k = c["k"]
+    w = np.array([[_f32_from_hex(h) for h in c["w_f32_bits"]]], dtype=np.float32)
+    # the bit patterns are the exact values the derivation names
+    assert [float(v) for v in w[0]] == [_exact(e) for e in c["w"]]
+    y = np.array([int(h, 16) for h in c["y_bf16_bits"]], dtype=np.uint16).reshape(k, 1, 1)
+    idx = np.arange(k, dtype=np.int32).reshape(1, k)
+    slot = np.zeros((1, k), dtype=np.int32)
+    out = O.combine(y, idx, w, slot, 1)
+    assert int(out[0, 0]) == int(c["out_bf16_bits"], 16)
+
+
+def test_expert_fp8_dequantise_then_scale_by_hand():
+    """The synthetic expert on fp8 rows, y = bf16((q * scale) * s_e) in two fp32 products in that
+    order ("dequant(x) * s_e"): a hand-derived element whose result differs from q * (scale * s_e)."""
+    c = _order_golden()["expert_fp8"][0]
+    H = c["H"]
+    scale = _f32_from_hex(c["scale_f32_bits"])
+    s_e = _f32_from_hex(c["s_e_f32_bits"])
+    assert float(scale) == _exact(c["scale"]) and float(s_e) == _exact(c["s_e"])
+    code = int(c["code"], 16)
+    assert float(O.e4m3_decode(np.array([code], np.uint8))[0]) == _exact(c["q"])
+    recv = np.zeros((2, 1, H), dtype=np.uint8)
+    recv[1, 0, 0] = code
+    recv[1, 0, 1] = code | 0x80                  # the same value negated: the result's negation
+    recv_scale = np.full((2, 1, H // 128), scale, dtype=np.float32)
+    counts = np.array([0, 1], dtype=np.int32)
+    s = np.array([1.0, s_e], dtype=np.float32)
+    y = O.expert_synthetic(recv, recv_scale, counts, s)
+    want = int(c["y_bf16_bits"], 16)
+    assert int(y[1, 0, 0]) == want
+    assert int(y[1, 0, 1]) == want | 0x8000
+    assert np.all(y[1, 0, 2:] == 0)
+
+
 # ---- dual batch overlap split ------------------------------------------------------
 
 def test_micro_batch_split_at_midpoint():
