@@ -1,27 +1,46 @@
 // moe_abi.cu -- status strings, argument validation and workspace sizing.
-// Host code only; nothing here touches the GPU except the cached SM count.
+// Host code only; nothing here touches the GPU except the cached SM count,
+// the status word's address and the current context's identity.
 #include "moe_internal.cuh"
 
-#include <mutex>
+#include <cuda.h>
 
 namespace moe {
 
 namespace {
 __device__ unsigned g_device_status;    // kStatus* bits, set by kernels whose bounded waits gave up
-std::mutex g_status_mutex;
-unsigned *g_status_addr[64] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_fn(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
 }  // namespace
 
+bool current_ctx(CtxKey *key) {
+    static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (get_current == nullptr || get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (cudaGetDevice(&key->dev) != cudaSuccess) return false;
+    // before the runtime's first call on this thread no context may be current yet
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, &key->id) == CUDA_SUCCESS;
+}
+
 unsigned *device_status_word() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(g_status_mutex);
-    if (g_status_addr[dev] == nullptr) {
+    static PerContext<unsigned *> cache;
+    return cache.get([] {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-        g_status_addr[dev] = static_cast<unsigned *>(p);
-    }
-    return g_status_addr[dev];
+        return cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess ? static_cast<unsigned *>(p) : nullptr;
+    });
 }
 
 int check_problem(const moe_problem *p, Dims *d) {
@@ -47,16 +66,15 @@ int check_problem(const moe_problem *p, Dims *d) {
 }
 
 int sm_count() {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (cached[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-        cached[dev] = n;
-    }
-    return cached[dev];
+    static PerContext<int> cache;
+    const int n = cache.get([] {
+        int dev = 0, m = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&m, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || m <= 0)
+            return 0;
+        return m;
+    });
+    return n > 0 ? n : 1;
 }
 
 }  // namespace moe

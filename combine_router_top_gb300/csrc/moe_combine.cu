@@ -222,16 +222,9 @@ int launch_expert_fp8(const Dims &d, long long max_rows, cudaStream_t st, const 
     const long long units = max_rows * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const size_t smem = (size_t)kWarps * 32 * U * 32;
-    static bool smem_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    if (!smem_set[dev]) {
-        if (cudaFuncSetAttribute(expert_fp8_bulk_kernel<U>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
-        smem_set[dev] = true;
-    }
-    static int resident = resident_blocks(expert_fp8_bulk_kernel<U>, kBlock, smem);
+    static PerContext<int> smem_done, resident_cache;
+    if (!set_smem_once(smem_done, expert_fp8_bulk_kernel<U>, (int)smem)) return MOE_ERR_CUDA;
+    const int resident = resident_blocks_cached(resident_cache, expert_fp8_bulk_kernel<U>, kBlock, smem);
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
     if (launch_pdl_smem(expert_fp8_bulk_kernel<U>, grid, kBlock, smem, st, static_cast<const uint4 *>(recv), scale,
                         counts, s, static_cast<uint4 *>(y), d.E, d.C, d.H, segs) != cudaSuccess)
@@ -242,7 +235,8 @@ int launch_expert_fp8(const Dims &d, long long max_rows, cudaStream_t st, const 
 template <int U>
 int launch_expert_bf16(const Dims &d, long long max_rows, cudaStream_t st, const void *recv,
                        const int32_t *counts, const float *s, void *y) {
-    static int resident = resident_blocks(expert_bf16_kernel<U>, kBlock);
+    static PerContext<int> resident_cache;
+    const int resident = resident_blocks_cached(resident_cache, expert_bf16_kernel<U>, kBlock);
     const int segs = (d.H / 8 + 32 * U - 1) / (32 * U);
     const long long units = max_rows * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
@@ -295,7 +289,8 @@ template <int KMAX>
 int launch_combine(const moe::Dims &d, cudaStream_t st, const uint4 *y, const int32_t *idx, const float *w,
                    const int32_t *slot, uint4 *out) {
     using namespace moe;
-    static int resident = resident_blocks(combine_kernel<KMAX>, kBlock);
+    static PerContext<int> resident_cache;
+    const int resident = resident_blocks_cached(resident_cache, combine_kernel<KMAX>, kBlock);
     const int H8 = d.H / 8;
     const int segs = (H8 + 31) / 32;
     const long long units = (long long)d.T * segs;

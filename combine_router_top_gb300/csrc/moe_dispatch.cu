@@ -469,7 +469,8 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
 template <int U>
 int launch_fp8(const Dims &d, cudaStream_t st, const void *x, const int32_t *idx, const int32_t *slot, void *recv,
                float *scale, int32_t *src) {
-    static int resident = resident_blocks(dispatch_fp8_kernel<U>, kBlock);
+    static PerContext<int> resident_cache;
+    const int resident = resident_blocks_cached(resident_cache, dispatch_fp8_kernel<U>, kBlock);
     const int n_tasks = d.H / 16;
     const int segs = (n_tasks + 32 * U - 1) / (32 * U);
     const long long units = (long long)d.T * segs;
@@ -484,7 +485,8 @@ int launch_fp8(const Dims &d, cudaStream_t st, const void *x, const int32_t *idx
 template <int U>
 int launch_bf16(const Dims &d, cudaStream_t st, const void *x, const int32_t *idx, const int32_t *slot, void *recv,
                 int32_t *src) {
-    static int resident = resident_blocks(dispatch_bf16_kernel<U>, kBlock);
+    static PerContext<int> resident_cache;
+    const int resident = resident_blocks_cached(resident_cache, dispatch_bf16_kernel<U>, kBlock);
     const int H8 = d.H / 8;
     const int segs = (H8 + 32 * U - 1) / (32 * U);
     const long long units = (long long)d.T * segs;
@@ -518,7 +520,8 @@ extern "C" int moe_dispatch(const moe_problem *p, const void *x, const int32_t *
     unsigned *status = device_status_word();
     if (status == nullptr) return MOE_ERR_CUDA;
     if (fp8 && d.H % kFp8Seg == 0) {
-        static int resident = resident_blocks(dispatch_fp8_seg_kernel, kFp8SegThreads);
+        static PerContext<int> resident_cache;
+        const int resident = resident_blocks_cached(resident_cache, dispatch_fp8_seg_kernel, kFp8SegThreads);
         const long long units = (long long)d.T * (d.H / kFp8Seg);
         const int grid = d.max_blocks > 0 ? persistent_grid(units, resident, d.max_blocks)
                                           : (int)std::min<long long>(units, 1LL << 30);
@@ -599,16 +602,10 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
         rc = launch_route_topk(d, st, logits, topk_idx, topk_w, rank, tile_counts);
         if (rc != MOE_OK) return rc;
     }
-    static bool smem_set[2][64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    static PerContext<int> smem_done[2];
     auto kernel = fp8 ? route_dispatch_kernel<true> : route_dispatch_kernel<false>;
-    if (!smem_set[fp8][dev]) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 fused_smem_bytes(kFusedMaxHidden, kMaxExperts)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        smem_set[fp8][dev] = true;
-    }
+    if (!set_smem_once(smem_done[fp8], kernel, (int)fused_smem_bytes(kFusedMaxHidden, kMaxExperts)))
+        return MOE_ERR_CUDA;
     if (launch_pdl_smem(kernel, d.T + 1, kFusedThreads, fused_smem_bytes(d.H, d.E), st,
                         static_cast<const uint16_t *>(x), static_cast<const int32_t *>(topk_idx),
                         static_cast<const int32_t *>(rank), static_cast<const int32_t *>(tile_counts), slot,

@@ -565,15 +565,8 @@ int launch_gemm(const Dims &d, const void *recv, const float *recv_scale, const 
         return MOE_ERR_CUDA;
     unsigned *status = device_status_word();
     if (status == nullptr) return MOE_ERR_CUDA;
-    static bool smem_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-    if (!smem_set[dev]) {
-        if (cudaFuncSetAttribute(expert_gemm_kernel<FP8, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kGemmSmemBytes) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        smem_set[dev] = true;
-    }
+    static PerContext<int> smem_done;
+    if (!set_smem_once(smem_done, expert_gemm_kernel<FP8, WIDE>, (int)kGemmSmemBytes)) return MOE_ERR_CUDA;
     int grid = sm_count();                        // persistent: one CTA per SM
     if (d.max_blocks > 0 && d.max_blocks < grid) grid = d.max_blocks;
     if (launch_pdl_smem(expert_gemm_kernel<FP8, WIDE>, grid, kGemmThreads, kGemmSmemBytes, as_stream(stream), map_a,

@@ -11,7 +11,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <initializer_list>
+#include <mutex>
 
 #include "moe.h"
 
@@ -45,7 +47,65 @@ unsigned *device_status_word();
 // Bits of the device status word.
 constexpr unsigned kStatusWaitGaveUp = 1u;     // a bounded wait on a copy gave up
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-int sm_count();                         // SMs of the current device (cached)
+int sm_count();                         // SMs of the current device (cached per context)
+
+// The CUDA context current on the calling thread: its device and its unique
+// id (cuCtxGetId). A context created again after cudaDeviceReset gets a new
+// id. Returns false if there is no current context or the lookup fails.
+struct CtxKey {
+    int dev;
+    unsigned long long id;
+};
+bool current_ctx(CtxKey *key);
+
+// A value computed once per CUDA context and read without a lock afterwards.
+// Device addresses of this library's __device__ arrays, function attributes
+// and occupancy all belong to the context they were obtained in, so a
+// context re-created after cudaDeviceReset (or another context on the same
+// device) computes its own. `make` returns the value; a value equal to T{}
+// (0, nullptr) means failure and is returned without being cached. Records
+// are never freed (a reader may still hold one); there is one per context
+// seen, chained per device.
+template <typename T>
+class PerContext {
+    static constexpr int kDevices = 64;
+    struct Rec {
+        unsigned long long id;
+        T val;
+        const Rec *next;
+    };
+    std::atomic<const Rec *> head_[kDevices] = {};
+    std::mutex mu_;
+
+    const Rec *find(int dev, unsigned long long id) const {
+        for (const Rec *r = head_[dev].load(std::memory_order_acquire); r != nullptr; r = r->next)
+            if (r->id == id) return r;
+        return nullptr;
+    }
+
+  public:
+    template <typename F>
+    T get(F make) {
+        CtxKey k;
+        if (!current_ctx(&k) || k.dev < 0 || k.dev >= kDevices) return make();
+        if (const Rec *r = find(k.dev, k.id)) return r->val;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (const Rec *r = find(k.dev, k.id)) return r->val;
+        const T v = make();
+        if (v == T{}) return v;
+        head_[k.dev].store(new Rec{k.id, v, head_[k.dev].load(std::memory_order_relaxed)}, std::memory_order_release);
+        return v;
+    }
+};
+
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per
+// context; false if the runtime refuses it.
+template <typename Kernel>
+bool set_smem_once(PerContext<int> &done, Kernel kernel, int bytes) {
+    return done.get([&] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess ? 1 : 0;
+    }) == 1;
+}
 // The route's top-k / tile kernel alone (moe_route.cu), for n_tiles > 0.
 int launch_route_topk(const Dims &d, cudaStream_t st, const float *logits, int32_t *topk_idx, float *topk_w,
                       int32_t *rank, int32_t *tile_counts);
@@ -64,6 +124,12 @@ int resident_blocks(Kernel kernel, int block, size_t smem = 0) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess || n < 1) n = 1;
     return n * sm_count();
+}
+
+// resident_blocks, computed once per context into `cache`.
+template <typename Kernel>
+int resident_blocks_cached(PerContext<int> &cache, Kernel kernel, int block, size_t smem = 0) {
+    return cache.get([&] { return resident_blocks(kernel, block, smem); });
 }
 
 // Grid of a persistent kernel over `units` work units: one wave of resident

@@ -43,7 +43,8 @@ int layer_stand_in(const void *in, void *out, int64_t n_elements, float a, int32
     if (n_elements < 0 || n_elements % 8 != 0 || busy_fmas < 0 || busy_fmas > (1 << 20)) return MOE_ERR_INVALID_ARG;
     if (n_elements == 0) return MOE_OK;
     if (!in || !out || !aligned(in, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
-    static int resident = resident_blocks(stand_in_kernel, 256);
+    static PerContext<int> resident_cache;
+    const int resident = resident_blocks_cached(resident_cache, stand_in_kernel, 256);
     const long long n16 = n_elements / 8;
     const int grid = persistent_grid((n16 + 255) / 256, resident, max_blocks);
     if (launch_pdl(stand_in_kernel, grid, 256, st, static_cast<const uint4 *>(in), static_cast<uint4 *>(out), n16, a,

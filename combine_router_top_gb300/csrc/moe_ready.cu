@@ -231,7 +231,8 @@ int launch_expert_combine(const Dims &d, cudaStream_t st, const void *recv, cons
                           unsigned *status) {
     auto kernel = expert_combine_kernel<KMAX, FP8>;
     const size_t smem = FP8 ? (size_t)kRWarps * 32 * kSegTasks * 32 : 0;
-    static int resident = resident_blocks(kernel, kRBlock, smem);   // blocks resident on the whole GPU
+    static PerContext<int> resident_cache;     // blocks resident on the whole GPU
+    const int resident = resident_blocks_cached(resident_cache, kernel, kRBlock, smem);
     int grid = resident;
     if (d.max_blocks > 0 && d.max_blocks < grid) grid = d.max_blocks;
     if (grid < 2) return MOE_ERR_UNSUPPORTED;

@@ -24,8 +24,6 @@
 // two-level scan: route_chunk_sums adds each chunk of kChunkTiles tiles,
 // route_chunk_scan turns the chunk sums into exclusive bases, and K2 adds to
 // its chunk's base only the tiles before it in its own chunk.
-#include <mutex>
-
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -326,27 +324,19 @@ extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *top
 namespace {
 
 constexpr size_t kStaticRouteScratchBytes = 1u << 20;     // 1 MiB on every GPU that loads the library
-constexpr int kMaxScratchDevices = 64;
 
 __device__ __align__(256) unsigned char g_route_scratch[kStaticRouteScratchBytes];
 
-std::mutex g_scratch_mutex;
-void *g_scratch_addr[kMaxScratchDevices] = {};
-
-// Device address of g_route_scratch on the current device, looked up once per
-// device (the host-side name of the array is not a device address).
-int route_scratch_address(void **addr) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+// Device address of g_route_scratch in the current context, looked up once
+// per context (the host-side name of the array is not a device address, and
+// a context created again after cudaDeviceReset may load the array
+// elsewhere); nullptr if the lookup fails.
+void *route_scratch_address() {
+    static moe::PerContext<void *> cache;
+    return cache.get([] {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *addr = g_scratch_addr[dev];
-    return MOE_OK;
+        return cudaGetSymbolAddress(&p, g_route_scratch) == cudaSuccess ? p : nullptr;
+    });
 }
 
 }  // namespace
@@ -358,9 +348,8 @@ extern "C" int moe_route_noalloc(const moe_problem *p, const float *logits, int3
     const int rc = check_problem(p, nullptr);
     if (rc != MOE_OK) return rc;
     if (moe_route_workspace_bytes(p) > kStaticRouteScratchBytes) return MOE_ERR_UNSUPPORTED;
-    void *scratch = nullptr;
-    const int ac = route_scratch_address(&scratch);
-    if (ac != MOE_OK) return ac;
+    void *scratch = route_scratch_address();
+    if (scratch == nullptr) return MOE_ERR_CUDA;
     return moe_route(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_counts, dropped, scratch,
                      kStaticRouteScratchBytes, stream);
 }

@@ -151,10 +151,13 @@ int moe_route(const moe_problem *p, const float *logits,
  *  returns MOE_ERR_UNSUPPORTED, launching nothing, when the problem needs more
  *  (moe_route_workspace_bytes(p) > 1 MiB, about E x 4.25 bytes per tile of 32
  *  tokens; for instance more than 30784 tokens at E = 256).
- *  Set-up: the first call on a device looks up the array's device address
- *  with that device current (cudaGetSymbolAddress); make that first call
- *  before any stream capture on the device. Later calls do no CUDA call other
- *  than the kernel launches.
+ *  Set-up: the first call in a CUDA context looks up the array's device
+ *  address with that context current (cudaGetSymbolAddress); make that first
+ *  call before any stream capture on the device. The address is kept per
+ *  context: after cudaDeviceReset the re-created context looks it up again on
+ *  its first call. Later calls in the same context make no CUDA call other
+ *  than the kernel launches and the lock-free lookup of the current device
+ *  and context (cudaGetDevice, cuCtxGetCurrent, cuCtxGetId).
  *  Sharing: all calls on a device use the same array, which keeps the last
  *  call's contents (the route kernels overwrite what they read, so nothing
  *  needs clearing). Calls whose executions overlap on the GPU (other streams,

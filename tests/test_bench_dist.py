@@ -67,3 +67,34 @@ def test_traffic_records_follow_code_not_comments(tmp_path, monkeypatch):
     assert bench.kernel_source_sha(["k.cu"]) == a
     (csrc / "k.cu").write_text("__global__ void k(int *p) { p[0] = 2; }\n")
     assert bench.kernel_source_sha(["k.cu"]) != a
+
+
+@pytest.mark.parametrize("name,T,threads", [("dsv3_fp8", 200, 7), ("v2lite", 256, 5), ("tiny", 64, 64)])
+def test_threaded_oracle_baseline_equals_the_oracle_path(name, T, threads):
+    """The CPU baseline's threaded harness (the oracle's functions over disjoint token and expert
+    ranges) computes exactly what the single-threaded oracle path computes."""
+    import numpy as np
+    import bench
+    import oracle as O
+    import workloads as W
+    w = W.WORKLOADS[name]
+    x, lg, s = W.make_x(w, 0, T), W.make_logits(w, 0, T), W.expert_scale(w)
+    fp8 = w.dtype == W.DTYPE_FP8_E4M3_B128
+    ref = O.run_path(x, lg, s, w.k, w.R, w.C, fp8)
+    to = bench.ThreadedOracle(O, x, lg, s, w, threads)
+    try:
+        for _ in range(2):
+            to.step()
+            assert np.array_equal(to.idx, ref["topk_idx"]) and np.array_equal(to.wt, ref["topk_w"])
+            for key in ["counts", "offsets", "slot", "rank_counts"]:
+                assert np.array_equal(getattr(to, key), ref[key]), key
+            assert int(to.dropped[0]) == ref["dropped"]
+            assert np.array_equal(to.out, ref["out"])
+            for e, c in enumerate(ref["counts"].tolist()):
+                n = min(c, w.C)
+                assert np.array_equal(to.recv_src[e, :n], ref["recv_src"][e, :n])
+                assert np.array_equal(to.y[e, :n], ref["y"][e, :n])
+                assert np.array_equal(to.recv[e, :n], ref["recv_q" if fp8 else "recv_x"][e, :n])
+            to.recv_src.fill(-1)
+    finally:
+        to.close()

@@ -61,15 +61,36 @@ def test_noalloc_route_matches_route_on_two_calls_in_a_row(name):
         assert np.array_equal(got2["slot"], ref2["slot"]) and np.array_equal(got2["counts"], ref2["counts"])
 
 
+def test_noalloc_route_at_the_exact_scratch_limit():
+    """30784 tokens at 256 experts fill the array exactly: 962 tiles of 32 tokens take the two-level scan,
+    whose chunk sums and bases sit at the end of the 1 MiB. Bit for bit as moe_route, twice in a row."""
+    import torch
+    from combine_router_top_gb300 import build as B
+    B.build()
+    import combine_router_top_gb300 as M
+    w = W.WORKLOADS["dsv3_fp8"].with_(T=30784, C=2048, seed=4242)
+    p = M.problem(w.T, w.H, w.E, w.k, w.R, w.C, w.dtype)
+    assert M.moe_route_workspace_bytes(p) == (1 << 20)
+    logits = torch.from_numpy(W.make_logits(w)).to(DEV)
+    ref = route_outputs(M, p, logits, use_noalloc=False)
+    for _ in range(2):
+        got = route_outputs(M, p, logits, use_noalloc=True)
+        for key in ["topk_idx", "counts", "offsets", "slot", "rank_counts", "dropped"]:
+            assert np.array_equal(got[key], ref[key]), key
+        assert np.array_equal(got["topk_w"].view(np.uint32), ref["topk_w"].view(np.uint32))
+
+
 def test_noalloc_route_refuses_problems_beyond_its_scratch():
     import torch
     from combine_router_top_gb300 import build as B
     B.build()
     import combine_router_top_gb300 as M
-    # 131072 tokens at 256 experts need 4096 tiles x 256 x 4 bytes = 4 MiB > 1 MiB
-    p = M.problem(131072, 7168, 256, 8, 8, 1024)
-    assert M.moe_route_workspace_bytes(p) > (1 << 20)
+    # 131072 tokens at 256 experts need 4096 tiles x 256 x 4 bytes = 4 MiB > 1 MiB; 30785 tokens (963 tiles)
+    # need 1 KiB more than the array, one token past the largest batch that fits
     t = torch.zeros(16, dtype=torch.int32, device=DEV)
-    with pytest.raises(M.MoeError) as err:
-        M.moe_route_noalloc(p, t, t, t, t, t, t, t, t)
-    assert err.value.status == M.MOE_ERR_UNSUPPORTED
+    for T in [131072, 30785]:
+        p = M.problem(T, 7168, 256, 8, 8, 1024)
+        assert M.moe_route_workspace_bytes(p) > (1 << 20)
+        with pytest.raises(M.MoeError) as err:
+            M.moe_route_noalloc(p, t, t, t, t, t, t, t, t)
+        assert err.value.status == M.MOE_ERR_UNSUPPORTED
