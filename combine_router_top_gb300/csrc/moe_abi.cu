@@ -109,11 +109,16 @@ int moe_device_status(void) {
 size_t moe_route_workspace_bytes(const moe_problem *p) {
     moe::Dims d;
     if (moe::check_problem(p, &d) != MOE_OK) return 0;
-    const size_t tiles = ((size_t)d.T + moe::kTileTokens - 1) / moe::kTileTokens;
-    size_t bytes = tiles * (size_t)d.E * sizeof(int32_t);              // counts per (tile, expert)
-    if (moe::route_two_level(tiles, d.E)) {                            // + sums and bases per (chunk, expert)
-        const size_t chunks = (tiles + moe::kChunkTiles - 1) / moe::kChunkTiles;
-        bytes += 2 * chunks * (size_t)d.E * sizeof(int32_t);
+    size_t bytes;
+    if (moe::route_small(d.T)) {
+        bytes = (size_t)d.E * moe::route_small_stride(d.T);              // one byte per (expert, tile of 8)
+    } else {
+        const size_t tiles = ((size_t)d.T + moe::kTileTokens - 1) / moe::kTileTokens;
+        bytes = tiles * (size_t)d.E * sizeof(int32_t);                 // counts per (tile of 32, expert)
+        if (moe::route_two_level(tiles, d.E)) {                        // + sums and bases per (chunk, expert)
+            const size_t chunks = (tiles + moe::kChunkTiles - 1) / moe::kChunkTiles;
+            bytes += 2 * chunks * (size_t)d.E * sizeof(int32_t);
+        }
     }
     bytes = (bytes + 255) & ~(size_t)255;
     return bytes < 256 ? 256 : bytes;

@@ -298,54 +298,25 @@ dispatch_bf16_tma_kernel(const uint16_t *__restrict__ x, const int32_t *__restri
 
 // ---- fused route finalisation + dispatch, for decode-sized batches -----------
 //
-// The top-k kernel of moe_route leaves, per pair, its rank within its tile of
-// 32 tokens and, per tile, the count per expert. Here one block per token t
-// stages t's bf16 row in shared memory (one bulk copy, issued before the wait
-// on the top-k kernel: x is an input of the call, final when this grid
-// starts), forms the slots of t's k choices while the copy is in flight
-// (slot_j = rank_j + the counts of expert e_j in the tiles before t's tile,
-// the tiles split over the block's threads), writes slot[] and recv_src,
+// The small-batch top-k kernel of moe_route leaves, per pair, its rank within
+// its tile of 8 tokens (in slot[]) and, per (expert, tile), the tile's count as
+// one byte of cnt8[E][stride]. Here one block per token t stages t's bf16 row
+// in shared memory (one bulk copy, issued before the wait on the top-k kernel:
+// x is an input of the call, final when this grid starts), forms the slots of
+// t's k choices while the copy is in flight (slot_j = rank_j + the first
+// t/8 bytes of row e_j, one warp per choice), writes slot[] and recv_src,
 // then writes the row to each kept destination: for an fp8 dispatch each
 // thread stores the 16 codes it has just quantised (16-byte stores, coalesced
 // across the block), for a bf16 one the staged row leaves by one bulk store
-// per destination. Block 0 forms
-// counts, offsets, rank_counts and dropped from the tile counts.
-constexpr int kFusedMaxTiles = 32;             // decode-sized batches: at most 1024 tokens
+// per destination. Block 0 forms counts, offsets, rank_counts and dropped
+// from the byte counts.
+constexpr int kFusedMaxTokens = 1024;          // decode-sized batches
 constexpr int kFusedThreads = 256;             // two quantise passes at H 7168; 128, 384 and 512 measured no faster
 constexpr int kFusedMaxHidden = 16384;         // staged bf16 row: 2 * H bytes of shared memory
+static_assert(kFusedMaxTokens <= kRouteSmallMaxTokens, "the fused path runs on the small-batch top-k kernel");
 
 constexpr size_t fused_smem_bytes(int H, int E) {
     return 2 * (size_t)H > 4 * (size_t)E ? 2 * (size_t)H : 4 * (size_t)E;
-}
-
-// tot: E ints of shared memory
-__device__ void fused_totals(const int32_t *__restrict__ tile_counts, int n_tiles, int E, int R, int C,
-                             int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                             int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped, int32_t *tot) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int sum = 0;
-#pragma unroll 8
-        for (int b = 0; b < n_tiles; ++b) sum += __ldcg(tile_counts + (size_t)b * E + e);
-        tot[e] = sum;
-        counts[e] = sum;
-    }
-    __syncthreads();
-    const int per_rank = E / R;
-    for (int r = threadIdx.x; r < R; r += blockDim.x) {
-        int kept = 0;
-        for (int e = r * per_rank; e < (r + 1) * per_rank; ++e) kept += tot[e] < C ? tot[e] : C;
-        rank_counts[r] = kept;
-    }
-    if (threadIdx.x == 0) {
-        int run = 0, lost = 0;
-        for (int e = 0; e < E; ++e) {
-            offsets[e] = run;
-            run += tot[e];
-            lost += tot[e] > C ? tot[e] - C : 0;
-        }
-        offsets[E] = run;
-        *dropped = lost;
-    }
 }
 
 // FP8: quantise the staged row and store codes and scales; bf16: store the
@@ -353,7 +324,7 @@ __device__ void fused_totals(const int32_t *__restrict__ tile_counts, int n_tile
 template <bool FP8>
 __global__ void __launch_bounds__(kFusedThreads)
 route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
-                          const int32_t *__restrict__ rank, const int32_t *__restrict__ tile_counts,
+                          const uint8_t *__restrict__ cnt8, int stride,
                           int32_t *__restrict__ slot, uint8_t *__restrict__ recv_q, float *__restrict__ recv_scale,
                           int32_t *__restrict__ recv_src, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                           int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped, int H, int E, int k,
@@ -362,14 +333,15 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
     extern __shared__ __align__(128) uint4 fused_smem[];
     __shared__ float ss[kFusedMaxHidden / 128];
     __shared__ __align__(8) uint64_t bar;
-    __shared__ int s_part[kFusedThreads];
+    __shared__ int s_base[kMaxTopK];
     __shared__ int s_row[kMaxTopK];
+    __shared__ int s_wsum[32];
     __shared__ int s_n;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (blockIdx.x == 0) {          // the totals block: first, so that it is no tail of the grid
         pdl_enter();
-        fused_totals(tile_counts, n_tiles, E, R, C, counts, offsets, rank_counts, dropped,
-                     reinterpret_cast<int32_t *>(fused_smem));
+        small_route_totals(cnt8, (size_t)stride, n_tiles, E, R, C, counts, offsets, rank_counts, dropped,
+                           reinterpret_cast<int *>(fused_smem), s_wsum);
         return;
     }
     const int t = blockIdx.x - 1;
@@ -382,22 +354,21 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
         bulk_g2s(xs, x + (size_t)t * H, (uint32_t)H * 2, &bar);
     }
     pdl_wait();                 // top-k kernel complete from here on; dependents launch at the end
-    // slot of each choice j: rank + counts of e_j in the tiles before t's tile
-    const int tile = t / kTileTokens;
-    const int parts = kFusedThreads / k;
-    const int e = __ldg(topk_idx + (size_t)t * k + tid % k);
-    const int my_rank = tid < k ? __ldg(rank + (size_t)t * k + tid) : 0;
-    int sum = 0;
-    if (tid < parts * k) {
-        for (int b = tid / k; b < tile; b += parts) sum += __ldcg(tile_counts + (size_t)b * E + e);
+    // slot of each choice j: its rank in t's tile (in slot[]) + the pairs of e_j
+    // in the tiles before t's tile, the first t/8 bytes of row e_j (warp j % 8)
+    const int tile = t / kSmallTileTokens;
+    for (int j = warp; j < k; j += kFusedThreads / 32) {
+        const int ej = __ldg(topk_idx + (size_t)t * k + j);
+        const int pre = warp_row_prefix(cnt8 + (size_t)ej * stride, tile);
+        if (lane == 0) s_base[j] = pre;
     }
-    s_part[tid] = sum;
+    const int e = lane < k ? __ldg(topk_idx + (size_t)t * k + lane) : 0;
+    const int my_rank = (tid < k) ? slot[(size_t)t * k + tid] : 0;
     __syncthreads();
     if (tid < 32) {
         int dest = -1;
         if (lane < k) {
-            int base = my_rank;
-            for (int part = 0; part < parts; ++part) base += s_part[part * k + lane];
+            const int base = s_base[lane] + my_rank;
             const int sl = base < C ? base : -1;
             slot[(size_t)t * k + lane] = sl;
             if (sl >= 0) dest = e * C + sl;
@@ -557,11 +528,8 @@ extern "C" int moe_dispatch(const moe_problem *p, const void *x, const int32_t *
 extern "C" size_t moe_route_dispatch_workspace_bytes(const moe_problem *p) {
     moe::Dims d;
     if (moe::check_problem(p, &d) != MOE_OK) return 0;
-    const size_t tiles = ((size_t)d.T + moe::kTileTokens - 1) / moe::kTileTokens;
-    const size_t fused = (tiles * (size_t)d.E + (size_t)d.T * d.k) * sizeof(int32_t);
-    const size_t route = moe_route_workspace_bytes(p);
-    const size_t bytes = fused > route ? fused : route;
-    return (bytes + 255) & ~(size_t)255;
+    // the fused path uses the small-batch route's byte counts, the same workspace as moe_route
+    return moe_route_workspace_bytes(p);
 }
 
 extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, const void *x, int32_t *topk_idx,
@@ -574,8 +542,8 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
     if (rc != MOE_OK) return rc;
     if (workspace_bytes < moe_route_dispatch_workspace_bytes(p)) return MOE_ERR_INVALID_ARG;
     const bool fp8 = d.dtype == MOE_DTYPE_FP8_E4M3_B128;
-    const int n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
-    const bool fused = d.H <= kFusedMaxHidden && n_tiles <= kFusedMaxTiles && d.max_blocks == 0;
+    const int n_tiles = (d.T + kSmallTileTokens - 1) / kSmallTileTokens;
+    const bool fused = d.H <= kFusedMaxHidden && d.T <= kFusedMaxTokens && d.max_blocks == 0;
     if (!fused) {
         rc = moe_route(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_counts, dropped, workspace,
                        workspace_bytes, stream);
@@ -596,10 +564,9 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
     cudaStream_t st = as_stream(stream);
     unsigned *status = device_status_word();
     if (status == nullptr) return MOE_ERR_CUDA;
-    int32_t *tile_counts = static_cast<int32_t *>(workspace);
-    int32_t *rank = tile_counts + (size_t)n_tiles * d.E;
+    uint8_t *cnt8 = static_cast<uint8_t *>(workspace);
     if (n_tiles > 0) {
-        rc = launch_route_topk(d, st, logits, topk_idx, topk_w, rank, tile_counts);
+        rc = launch_route_topk_small(d, st, logits, topk_idx, topk_w, slot, cnt8);
         if (rc != MOE_OK) return rc;
     }
     static PerContext<int> smem_done[2];
@@ -608,7 +575,7 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
         return MOE_ERR_CUDA;
     if (launch_pdl_smem(kernel, d.T + 1, kFusedThreads, fused_smem_bytes(d.H, d.E), st,
                         static_cast<const uint16_t *>(x), static_cast<const int32_t *>(topk_idx),
-                        static_cast<const int32_t *>(rank), static_cast<const int32_t *>(tile_counts), slot,
+                        static_cast<const uint8_t *>(cnt8), (int)route_small_stride(d.T), slot,
                         static_cast<uint8_t *>(recv), recv_scale, recv_src, counts, offsets, rank_counts, dropped, d.H,
                         d.E, d.k, d.C, d.R, n_tiles, status) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -22,6 +22,21 @@ namespace moe {
 constexpr int kTileTokens = 32;    // tokens per route tile: one 32-bit mask word per expert
 constexpr int kChunkTiles = 32;    // route tiles per chunk of the two-level scan of tile counts
 
+// Batches of up to kRouteSmallMaxTokens tokens take the small-batch route: tiles
+// of kSmallTileTokens tokens (one warp each, one 256-thread block per tile), and
+// the count of every (expert, tile) stored as one byte in an expert-major
+// workspace cnt8[E][stride] (a tile holds at most 8 pairs of one expert). The
+// counts of all tiles before tile b of expert e are then the first b bytes of
+// row e: at most 512 bytes, one 16-byte piece per lane of a warp.
+constexpr int kSmallTileTokens = 8;
+constexpr int kRouteSmallMaxTokens = 4096;
+inline bool route_small(long long T) { return T <= kRouteSmallMaxTokens; }
+// Bytes per expert row of the small-batch workspace: the tile count rounded up to 16.
+inline size_t route_small_stride(long long T) {
+    const size_t tiles = ((size_t)T + kSmallTileTokens - 1) / kSmallTileTokens;
+    return (tiles + 15) & ~(size_t)15;
+}
+
 // The route finaliser sums the counts of all earlier tiles directly, about
 // n_tiles^2 * E / 2 loads in all; above 2^22 of them (128 tiles at E = 256)
 // the two-level scan, two launches more but linear, is faster.
@@ -106,9 +121,11 @@ bool set_smem_once(PerContext<int> &done, Kernel kernel, int bytes) {
         return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess ? 1 : 0;
     }) == 1;
 }
-// The route's top-k / tile kernel alone (moe_route.cu), for n_tiles > 0.
-int launch_route_topk(const Dims &d, cudaStream_t st, const float *logits, int32_t *topk_idx, float *topk_w,
-                      int32_t *rank, int32_t *tile_counts);
+// The small-batch route's top-k kernel alone (moe_route.cu), for
+// 0 < T <= kRouteSmallMaxTokens: indices, weights, each pair's rank within its
+// tile of 8 tokens, and the byte counts cnt8[E][route_small_stride(T)].
+int launch_route_topk_small(const Dims &d, cudaStream_t st, const float *logits, int32_t *topk_idx, float *topk_w,
+                            int32_t *rank, uint8_t *cnt8);
 // moe_layer_stand_in with a cap on its grid (moe_layers.cu).
 int layer_stand_in(const void *in, void *out, int64_t n_elements, float a, int32_t busy_fmas, int max_blocks,
                    cudaStream_t st);
@@ -396,6 +413,110 @@ __device__ __forceinline__ void quantise16_e4m3(const uint32_t wv[8], float sc, 
 // Total order on fp32 logits as unsigned keys: larger logit -> larger key,
 // -0.0 folded onto +0.0, NaN mapped to 1 (below every number), 0 reserved
 // for "no candidate".
+// ---- small-batch route helpers ------------------------------------------------
+
+// acc + the sum of the bytes of v (the 16 bytes at row offsets first .. first+15)
+// whose row offset is below limit, by shifts and masks.
+__device__ __forceinline__ unsigned add_bytes_below(uint4 v, int first, int limit, unsigned acc) {
+    const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int n = limit - (first + 4 * i);                  // valid bytes of word i
+        const unsigned m = n >= 4 ? 0xFFFFFFFFu : (n <= 0 ? 0u : (1u << (8 * n)) - 1u);
+        const unsigned x = w[i] & m;
+        const unsigned h = (x & 0x00FF00FFu) + ((x >> 8) & 0x00FF00FFu);    // two 16-bit partial sums
+        acc += (h & 0xFFFFu) + (h >> 16);
+    }
+    return acc;
+}
+
+// Sum of v over the 32 lanes of a warp, by a butterfly of shuffles; every lane
+// returns it. The byte sums of the small-batch route are reduced this way: in a
+// probe on sm_103a (nvcc 13.0) the same sums reduced with redux.sync
+// (__reduce_add_sync) came out wrong, while each lane's value was right.
+__device__ __forceinline__ unsigned warp_sum(unsigned v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// Sum of bytes [0, limit) of a 16-byte aligned row, limit <= 512, over one warp:
+// lane l reads bytes [16 l, 16 l + 16). Every lane returns the sum.
+__device__ __forceinline__ int warp_row_prefix(const uint8_t *__restrict__ row, int limit) {
+    const int c = (threadIdx.x & 31) * 16;
+    unsigned acc = 0;
+    if (c < limit) acc = add_bytes_below(__ldcg(reinterpret_cast<const uint4 *>(row + c)), c, limit, 0u);
+    return (int)warp_sum(acc);
+}
+
+// One block (any multiple of 32 threads, at most 1024) turns the byte counts
+// cnt8[E][stride] of n_tiles tiles into the totals: counts[e], offsets[0..E]
+// (exclusive scan), rank_counts[r] (kept rows of the experts of rank r) and
+// dropped. tot: E ints, wsum: 32 ints, both shared.
+__device__ inline void small_route_totals(const uint8_t *__restrict__ cnt8, size_t stride, int n_tiles, int E, int R,
+                                          int C, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                          int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped, int *tot,
+                                          int *wsum) {
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += nt) {
+        const uint8_t *row = cnt8 + (size_t)e * stride;
+        unsigned acc = 0;
+#pragma unroll 8
+        for (int c = 0; c < n_tiles; c += 16)
+            acc = add_bytes_below(__ldcg(reinterpret_cast<const uint4 *>(row + c)), c, n_tiles, acc);
+        tot[e] = (int)acc;
+        counts[e] = (int)acc;
+    }
+    __syncthreads();
+    // exclusive scan of tot over e: each thread a run of consecutive experts
+    const int per = (E + nt - 1) / nt;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int local = 0, lost = 0;
+    for (int e = e0; e < e1; ++e) {
+        local += tot[e];
+        lost += tot[e] > C ? tot[e] - C : 0;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += n;
+    }
+    lost = (int)warp_sum((unsigned)lost);
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < (nt >> 5) ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += n;
+        }
+        wsum[lane] = v;
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int e = e0; e < e1; ++e) {
+        offsets[e] = run;
+        run += tot[e];
+    }
+    if (tid == nt - 1) offsets[E] = run;
+    const int per_rank = E / R;
+    for (int r = tid; r < R; r += nt) {
+        int kept = 0;
+        for (int e = r * per_rank; e < (r + 1) * per_rank; ++e) kept += tot[e] < C ? tot[e] : C;
+        rank_counts[r] = kept;
+    }
+    __syncthreads();                           // every read of wsum above is done
+    if (lane == 0) wsum[warp] = lost;
+    __syncthreads();
+    if (tid == 0) {
+        int d = 0;
+        for (int w = 0; w < (nt >> 5); ++w) d += wsum[w];
+        *dropped = d;
+    }
+}
+
 __device__ __forceinline__ uint32_t logit_key(float f) {
     uint32_t u = __float_as_uint(f);
     if (f != f) return 1u;

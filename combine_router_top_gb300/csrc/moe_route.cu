@@ -8,28 +8,89 @@
 // bound lets every sender compute a unique destination address.
 //
 // Two launches (the second a programmatic dependent of the first, so its
-// launch latency hides behind the first), no atomics that decide an order:
-//   K1 route_topk_tile: one CTA per tile of 32 tokens, one warp per token.
-//      Top-k by k rounds of a warp arg-max (redux.sync max on an order-
-//      preserving 32-bit key, ballot for the lowest tied lane). Weights by
-//      expf and one IEEE division. Each chosen expert sets the token's bit in
-//      a per-expert 32-bit shared-memory mask; a pair's rank within the tile is
-//      the popcount of the lower bits, the tile's count per expert the popcount.
-//   K2 route_finalize: one CTA per tile. The tile's per-expert base is the
-//      sum of the earlier tiles' counts; slot = base + rank in tile, or -1 at
-//      or past the capacity. The last CTA also forms the totals, offsets,
-//      rank counts and drops.
-// The sum over earlier tiles grows with the square of the batch; once it is
-// large (route_two_level), two more launches between K1 and K2 make it a
-// two-level scan: route_chunk_sums adds each chunk of kChunkTiles tiles,
-// route_chunk_scan turns the chunk sums into exclusive bases, and K2 adds to
-// its chunk's base only the tiles before it in its own chunk.
+// launch latency hides behind the first), no atomics that decide an order.
+// Small batches (T <= kRouteSmallMaxTokens, every decode batch):
+//   K1 route_topk_small: one 256-thread CTA per tile of 8 tokens, one warp per
+//      token (warp_topk: k rounds of a warp arg-max). Each chosen expert sets
+//      the token's bit in a per-expert shared-memory mask: a pair's rank within
+//      the tile is the popcount of the lower bits, the tile's count of expert e
+//      the popcount, stored as byte cnt8[e][tile].
+//   K2 route_slots_small: block 0 forms counts, offsets, rank_counts and
+//      dropped from the byte counts; block 1 + b takes tile b, one warp per
+//      token: the pairs of e_j in earlier tiles are the first b bytes of row
+//      e_j, summed by the warp in one 16-byte load per lane and a shuffle sum.
+// Large batches: the same top-k on tiles of 32 tokens (route_topk_tile) with
+// 32-bit counts per (tile, expert), then route_finalize, one CTA per tile,
+// adds the earlier tiles' counts; the last CTA forms the totals. That sum
+// grows with the square of the batch; once it is large (route_two_level), two
+// more launches between them make it a two-level scan: route_chunk_sums adds
+// each chunk of kChunkTiles tiles, route_chunk_scan turns the chunk sums into
+// exclusive bases, and route_finalize adds to its chunk's base only the tiles
+// before it in its own chunk.
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
 
-// Lane l of a token's warp owns experts [l*V, l*V + V) (clipped to E).
+// Top-k of one token by its warp. Lane l owns experts [l*V, l*V + V) (clipped
+// to E) of the token's logit row. k rounds of a warp arg-max: redux.sync max on
+// an order-preserving 32-bit key (-0 folded onto +0, NaN below every number),
+// then a ballot picks the lowest tied lane, which holds the lowest index.
+// Lane j < k returns choice j: its expert and its weight
+// w_j = exp(l_j - l_0) / sum_{i<k} exp(l_i - l_0) (expf, one IEEE division).
+template <int V>
+__device__ __forceinline__ void warp_topk(const float *__restrict__ row, int E, int k, int lane, int &my_e,
+                                          float &my_w) {
+    const int e0 = lane * V;
+    uint32_t key[V];
+    if ((V % 4) == 0 && (E % 4) == 0 && e0 + V <= E) {
+#pragma unroll
+        for (int i = 0; i < V; i += 4) {
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(row + e0 + i));
+            key[i] = logit_key(f.x);
+            key[i + 1] = logit_key(f.y);
+            key[i + 2] = logit_key(f.z);
+            key[i + 3] = logit_key(f.w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < V; ++i) key[i] = (e0 + i < E) ? logit_key(__ldg(row + e0 + i)) : 0u;
+    }
+
+    uint32_t my_key = 0, top_key = 0;
+    my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        // the lane's best remaining candidate (lowest index among equals)
+        uint32_t best = 0;
+        int bi = 0;
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            if (key[i] > best) { best = key[i]; bi = i; }
+        const uint32_t m = __reduce_max_sync(kFull, best);
+        // lanes own ascending index ranges: the lowest tied lane holds the lowest index
+        const int wl = __ffs(__ballot_sync(kFull, best == m)) - 1;
+        const int e = __shfl_sync(kFull, e0 + bi, wl);
+        if (lane == wl) {
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                if (i == bi) key[i] = 0u;
+        }
+        if (lane == j) { my_key = m; my_e = e; }
+        if (j == 0) top_key = m;
+    }
+
+    float ex = 0.0f;
+    if (lane < k) ex = expf(key_logit(my_key) - key_logit(top_key));
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    my_w = __fdiv_rn(ex, sum);
+}
+
+// Large batches, K1: one CTA per tile of 32 tokens, one warp per token. Each
+// chosen expert sets the token's bit in a per-expert 32-bit shared-memory
+// mask; a pair's rank within the tile is the popcount of the lower bits, the
+// tile's count per expert the popcount.
 template <int V>
 __global__ void __launch_bounds__(1024, 1)
 route_topk_tile_kernel(const float *__restrict__ logits, int T, int E, int k,
@@ -47,53 +108,11 @@ route_topk_tile_kernel(const float *__restrict__ logits, int T, int E, int k,
 
     int my_e = 0;
     if (active) {
-        const int e0 = lane * V;
-        const float *row = logits + (size_t)t * E;
-        uint32_t key[V];
-        if ((V % 4) == 0 && (E % 4) == 0 && e0 + V <= E) {
-#pragma unroll
-            for (int i = 0; i < V; i += 4) {
-                const float4 f = __ldg(reinterpret_cast<const float4 *>(row + e0 + i));
-                key[i] = logit_key(f.x);
-                key[i + 1] = logit_key(f.y);
-                key[i + 2] = logit_key(f.z);
-                key[i + 3] = logit_key(f.w);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < V; ++i) key[i] = (e0 + i < E) ? logit_key(__ldg(row + e0 + i)) : 0u;
-        }
-
-        uint32_t my_key = 0, top_key = 0;
-        for (int j = 0; j < k; ++j) {
-            // the lane's best remaining candidate (lowest index among equals)
-            uint32_t best = 0;
-            int bi = 0;
-#pragma unroll
-            for (int i = 0; i < V; ++i)
-                if (key[i] > best) { best = key[i]; bi = i; }
-            const uint32_t m = __reduce_max_sync(kFull, best);
-            // lanes own ascending index ranges: the lowest tied lane holds the lowest index
-            const int wl = __ffs(__ballot_sync(kFull, best == m)) - 1;
-            const int e = __shfl_sync(kFull, e0 + bi, wl);
-            if (lane == wl) {
-#pragma unroll
-                for (int i = 0; i < V; ++i)
-                    if (i == bi) key[i] = 0u;
-            }
-            if (lane == j) { my_key = m; my_e = e; }
-            if (j == 0) top_key = m;
-        }
-
-        // w_j = exp(l_j - l_0) / sum_{i<k} exp(l_i - l_0)
-        float ex = 0.0f;
-        if (lane < k) ex = expf(key_logit(my_key) - key_logit(top_key));
-        float sum = ex;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+        float my_w;
+        warp_topk<V>(logits + (size_t)t * E, E, k, lane, my_e, my_w);
         if (lane < k) {
             topk_idx[(size_t)t * k + lane] = my_e;
-            topk_w[(size_t)t * k + lane] = __fdiv_rn(ex, sum);
+            topk_w[(size_t)t * k + lane] = my_w;
             atomicOr(&mask[my_e], 1u << wt);
         }
     }
@@ -102,6 +121,91 @@ route_topk_tile_kernel(const float *__restrict__ logits, int T, int E, int k,
         slot_rank[(size_t)t * k + lane] = __popc(mask[my_e] & ((1u << wt) - 1u));
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         tile_counts[(size_t)tile * E + e] = __popc(mask[e]);
+}
+
+// Small batches, K1: one 256-thread CTA per tile of 8 tokens, one warp per
+// token, so that a decode batch spreads over most SMs. As the large-batch K1,
+// with 8-bit masks; the tile's count of expert e goes to byte cnt8[e][tile].
+template <int V>
+__global__ void __launch_bounds__(kSmallTileTokens * 32)
+route_topk_small_kernel(const float *__restrict__ logits, int T, int E, int k, int32_t *__restrict__ topk_idx,
+                        float *__restrict__ topk_w, int32_t *__restrict__ slot_rank, uint8_t *__restrict__ cnt8,
+                        int stride) {
+    __shared__ uint32_t mask[kMaxExperts];
+    pdl_enter();
+    const int lane = threadIdx.x & 31;
+    const int wt = threadIdx.x >> 5;                 // token within the tile
+    const int tile = blockIdx.x;
+    const int t = tile * kSmallTileTokens + wt;
+    const bool active = t < T;                       // warp-uniform
+    for (int e = threadIdx.x; e < E; e += blockDim.x) mask[e] = 0u;
+    __syncthreads();
+
+    int my_e = 0;
+    if (active) {
+        float my_w;
+        warp_topk<V>(logits + (size_t)t * E, E, k, lane, my_e, my_w);
+        if (lane < k) {
+            topk_idx[(size_t)t * k + lane] = my_e;
+            topk_w[(size_t)t * k + lane] = my_w;
+            atomicOr(&mask[my_e], 1u << wt);
+        }
+    }
+    __syncthreads();
+    if (active && lane < k)
+        slot_rank[(size_t)t * k + lane] = __popc(mask[my_e] & ((1u << wt) - 1u));
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        cnt8[(size_t)e * stride + tile] = (uint8_t)__popc(mask[e]);
+}
+
+// Small batches, K2: block 0 forms the totals (counts, offsets, rank_counts,
+// dropped) from all tiles' byte counts; block 1 + b finalises tile b, one warp
+// per token: for each choice j the warp sums the first b bytes of row e_j (the
+// pairs of e_j in earlier tiles), and slot = that + the rank within the tile,
+// or -1 at or past the capacity.
+__global__ void __launch_bounds__(kSmallTileTokens * 32)
+route_slots_small_kernel(int T, int n_tiles, int E, int k, int R, int C, const uint8_t *__restrict__ cnt8, int stride,
+                         const int32_t *__restrict__ topk_idx, int32_t *__restrict__ slot,
+                         int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                         int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped) {
+    __shared__ int tot[kMaxExperts];
+    __shared__ int wsum[32];
+    pdl_enter();
+    if (blockIdx.x == 0) {             // first, so that it is no tail of the grid
+        small_route_totals(cnt8, (size_t)stride, n_tiles, E, R, C, counts, offsets, rank_counts, dropped, tot, wsum);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    const int tile = blockIdx.x - 1;
+    const int t = tile * kSmallTileTokens + (threadIdx.x >> 5);
+    if (t >= T) return;                              // warp-uniform
+    const int e = lane < k ? __ldg(topk_idx + (size_t)t * k + lane) : 0;
+    const int rank = lane < k ? slot[(size_t)t * k + lane] : 0;
+    const int limit = tile;                          // bytes [0, tile) of a row: the earlier tiles
+    const int c = lane * 16;
+    unsigned part[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        part[j] = 0;
+        if (j < k) {                                 // warp-uniform
+            const int ej = __shfl_sync(kFull, e, j);
+            if (c < limit)
+                part[j] = add_bytes_below(__ldcg(reinterpret_cast<const uint4 *>(cnt8 + (size_t)ej * stride + c)),
+                                          c, limit, 0u);
+        }
+    }
+    int base = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if (j < k) {
+            const int sj = (int)warp_sum(part[j]);
+            if (lane == j) base = sj;
+        }
+    }
+    if (lane < k) {
+        const int sl = base + rank;
+        slot[(size_t)t * k + lane] = sl < C ? sl : -1;
+    }
 }
 
 // Chunk c of kChunkTiles tiles: chunk_sums[c][e] = the sum of its tiles'
@@ -235,21 +339,30 @@ cudaError_t launch_topk(int n_tiles, cudaStream_t st, const float *logits, const
     return launch_pdl(route_topk_tile_kernel<V>, n_tiles, 1024, st, logits, d.T, d.E, d.k, idx, w, slot, wc);
 }
 
+template <int V>
+cudaError_t launch_topk_small(int n_tiles, cudaStream_t st, const float *logits, const Dims &d, int32_t *idx,
+                              float *w, int32_t *rank, uint8_t *cnt8, int stride) {
+    return launch_pdl(route_topk_small_kernel<V>, n_tiles, kSmallTileTokens * 32, st, logits, d.T, d.E, d.k, idx, w,
+                      rank, cnt8, stride);
+}
+
 }  // namespace
 
-// The top-k / tile kernel alone (n_tiles > 0): top-k indices and weights, each
-// pair's rank within its tile into `rank`, per-tile counts into `tile_counts`.
-int launch_route_topk(const Dims &d, cudaStream_t st, const float *logits, int32_t *topk_idx, float *topk_w,
-                      int32_t *rank, int32_t *tile_counts) {
-    const int n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
+// The small-batch top-k kernel alone (T <= kRouteSmallMaxTokens, T > 0): top-k
+// indices and weights, each pair's rank within its tile of 8 tokens into
+// `rank`, and the byte counts cnt8[E][route_small_stride(T)] of every tile.
+int launch_route_topk_small(const Dims &d, cudaStream_t st, const float *logits, int32_t *topk_idx, float *topk_w,
+                            int32_t *rank, uint8_t *cnt8) {
+    const int n_tiles = (d.T + kSmallTileTokens - 1) / kSmallTileTokens;
+    const int stride = (int)route_small_stride(d.T);
     const int per_lane = (d.E + 31) / 32;
     cudaError_t e;
-    if (per_lane <= 1) e = launch_topk<1>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
-    else if (per_lane <= 2) e = launch_topk<2>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
-    else if (per_lane <= 4) e = launch_topk<4>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
-    else if (per_lane <= 8) e = launch_topk<8>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
-    else if (per_lane <= 16) e = launch_topk<16>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
-    else e = launch_topk<32>(n_tiles, st, logits, d, topk_idx, topk_w, rank, tile_counts);
+    if (per_lane <= 1) e = launch_topk_small<1>(n_tiles, st, logits, d, topk_idx, topk_w, rank, cnt8, stride);
+    else if (per_lane <= 2) e = launch_topk_small<2>(n_tiles, st, logits, d, topk_idx, topk_w, rank, cnt8, stride);
+    else if (per_lane <= 4) e = launch_topk_small<4>(n_tiles, st, logits, d, topk_idx, topk_w, rank, cnt8, stride);
+    else if (per_lane <= 8) e = launch_topk_small<8>(n_tiles, st, logits, d, topk_idx, topk_w, rank, cnt8, stride);
+    else if (per_lane <= 16) e = launch_topk_small<16>(n_tiles, st, logits, d, topk_idx, topk_w, rank, cnt8, stride);
+    else e = launch_topk_small<32>(n_tiles, st, logits, d, topk_idx, topk_w, rank, cnt8, stride);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -275,9 +388,26 @@ extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *top
         return MOE_ERR_INVALID_ARG;
 
     cudaStream_t st = as_stream(stream);
+    if (route_small(d.T)) {
+        // small batches: top-k per tile of 8 tokens, then slots and totals; the
+        // second kernel is a programmatic dependent of the first
+        uint8_t *cnt8 = static_cast<uint8_t *>(workspace);
+        const int n_tiles = (d.T + kSmallTileTokens - 1) / kSmallTileTokens;
+        if (n_tiles > 0) {
+            rc = launch_route_topk_small(d, st, logits, topk_idx, topk_w, slot, cnt8);
+            if (rc != MOE_OK) return rc;
+        }
+        // an empty batch still runs the totals block: it writes the zero counts
+        if (launch_pdl(route_slots_small_kernel, n_tiles + 1, kSmallTileTokens * 32, st, d.T, n_tiles, d.E, d.k, d.R,
+                       d.C, static_cast<const uint8_t *>(cnt8), (int)route_small_stride(d.T),
+                       static_cast<const int32_t *>(topk_idx), slot, counts, offsets, rank_counts,
+                       dropped) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
     int32_t *wc = static_cast<int32_t *>(workspace);
     const int n_tiles = (d.T + kTileTokens - 1) / kTileTokens;
-    if (n_tiles > 0) {
+    {
         const int per_lane = (d.E + 31) / 32;
         cudaError_t e;
         if (per_lane <= 1) e = launch_topk<1>(n_tiles, st, logits, d, topk_idx, topk_w, slot, wc);
@@ -303,10 +433,9 @@ extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *top
             return MOE_ERR_CUDA;
         chunk_base = bases;
     }
-    // an empty batch still runs one finalise block: it writes the zero counts.
-    // Launched as a programmatic dependent of the kernel before it: its launch
-    // latency overlaps that kernel's run.
-    if (launch_pdl(route_finalize_kernel, n_tiles > 0 ? n_tiles : 1, 1024, st, d.T, n_tiles, d.E, d.k, d.R, d.C,
+    // launched as a programmatic dependent of the kernel before it: its launch
+    // latency overlaps that kernel's run
+    if (launch_pdl(route_finalize_kernel, n_tiles, 1024, st, d.T, n_tiles, d.E, d.k, d.R, d.C,
                    static_cast<const int32_t *>(wc), chunk_base, static_cast<const int32_t *>(topk_idx), slot,
                    counts, offsets, rank_counts, dropped) != cudaSuccess)
         return MOE_ERR_CUDA;

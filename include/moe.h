@@ -104,11 +104,13 @@ int moe_device_status(void);
 int moe_validate(const moe_problem *p);
 
 /* Bytes of device workspace moe_route needs for this problem (host-only, no
- * CUDA call); 0 if the problem is invalid. The workspace holds one 32-bit
- * count per (tile of 32 tokens, expert) and, for large batches (more than
- * 2^22 / E tiles squared: 4096 tokens at E = 256), two 32-bit values per
- * (chunk of 32 tiles, expert) for a two-level scan of those counts. Its
- * contents need no initialisation. */
+ * CUDA call); 0 if the problem is invalid. Up to 4096 tokens the workspace
+ * holds one byte per (expert, tile of 8 tokens), each expert's row rounded up
+ * to 16 bytes: E * 16 * ceil(ceil(T/8) / 16) bytes. Beyond, it holds one
+ * 32-bit count per (tile of 32 tokens, expert) and, for large batches (more
+ * than 2^22 / E tiles squared), two 32-bit values per (chunk of 32 tiles,
+ * expert) for a two-level scan of those counts. Always a multiple of 256 and
+ * at least 256. Its contents need no initialisation. */
 size_t moe_route_workspace_bytes(const moe_problem *p);
 
 /* Step 1 and 2: router top-k with renormalised softmax weights, then the
@@ -193,8 +195,9 @@ int moe_dispatch(const moe_problem *p, const void *x,
  * that forms the token's slots from the per-tile counts and dispatches its
  * row (launched as a programmatic dependent of the first). Otherwise it calls
  * moe_route and moe_dispatch. workspace: device scratch of at least
- * moe_route_dispatch_workspace_bytes(p) bytes, 16-byte aligned, contents
- * needing no initialisation, not shared with a concurrent call. */
+ * moe_route_dispatch_workspace_bytes(p) bytes (equal to
+ * moe_route_workspace_bytes(p)), 16-byte aligned, contents needing no
+ * initialisation, not shared with a concurrent call. */
 size_t moe_route_dispatch_workspace_bytes(const moe_problem *p);
 int moe_route_dispatch(const moe_problem *p, const float *logits, const void *x,
                        int32_t *topk_idx, float *topk_w,

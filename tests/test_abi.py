@@ -82,24 +82,26 @@ def test_validate_accepts_workloads(moe):
 
 
 def test_route_workspace_bytes(moe):
-    p = mk(moe)        # 1024 tokens -> 32 tiles of 32, 256 experts, int32
-    assert moe.moe_route_workspace_bytes(p) == 32 * 256 * 4
-    # while tiles^2 * E <= 2^22 the finaliser sums earlier tiles directly (128
-    # tiles at E = 256); beyond, the two-level scan adds a sum and a base per
-    # (chunk of 32 tiles, expert)
-    assert moe.moe_route_workspace_bytes(mk(moe, T=4096)) == 128 * 256 * 4
+    # up to 4096 tokens: one byte per (expert, tile of 8 tokens), each expert's row
+    # rounded up to 16 bytes: 1024 tokens -> 128 tiles, 256 experts
+    p = mk(moe)
+    assert moe.moe_route_workspace_bytes(p) == 256 * 128
+    assert moe.moe_route_workspace_bytes(mk(moe, T=4096)) == 256 * 512
+    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=500, k=5, R=4)) == (500 * 416 + 255) // 256 * 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=100, k=5, R=4)) == (100 * 416 + 255) // 256 * 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=9, E=3, k=1, R=1)) == 256
+    # beyond: int32 counts per (tile of 32 tokens, expert); while tiles^2 * E <= 2^22
+    # the finaliser sums earlier tiles directly, beyond that the two-level scan adds
+    # a sum and a base per (chunk of 32 tiles, expert)
     assert moe.moe_route_workspace_bytes(mk(moe, T=4097)) == (129 + 2 * 5) * 256 * 4
-    # rounded up to a multiple of 256 bytes
-    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=500, k=5, R=4)) == ((102 + 2 * 4) * 500 * 4 + 255) // 256 * 256
-    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=100, k=5, R=4)) == (102 * 100 * 4 + 255) // 256 * 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=4097, E=8, R=8)) == (129 * 8 * 4 + 255) // 256 * 256
     assert moe.moe_route_workspace_bytes(mk(moe, T=0)) == 256
     assert moe.moe_route_workspace_bytes(mk(moe, T=33, E=8, R=2)) % 256 == 0
 
 
 def test_route_dispatch_workspace_bytes(moe):
-    p = mk(moe)        # 32 tiles x 256 experts of tile counts + 1024 x 8 ranks, int32
-    assert moe.moe_route_dispatch_workspace_bytes(p) == (32 * 256 + 1024 * 8) * 4
-    assert moe.moe_route_dispatch_workspace_bytes(p) >= moe.moe_route_workspace_bytes(p)
+    p = mk(moe)        # the fused path keeps its ranks in slot[]: the route's own workspace
+    assert moe.moe_route_dispatch_workspace_bytes(p) == moe.moe_route_workspace_bytes(p) == 256 * 128
     assert moe.moe_route_dispatch_workspace_bytes(mk(moe, T=0)) == 256
     assert moe.moe_route_dispatch_workspace_bytes(mk(moe, k=0)) == 0
     L = moe.lib()
