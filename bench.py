@@ -159,8 +159,61 @@ def ncu_traffic(kernel: str, workload: str):
     return None
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's libnvidia-ml, read-only queries)
+    every 2 ms on a thread, so that even a timed region of a few milliseconds holds samples."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_uuid: str, period_s: float = 0.002):
+        import ctypes
+        self.rows = []
+        self.period = period_s
+        self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.nv.nvmlDeviceGetHandleByUUID(gpu_uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle for " + gpu_uuid)
+        self.reason_fn = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 else None
+        self.stop_flag = threading.Event()
+
+    def _read(self):
+        import ctypes
+        mhz, why = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            ok = self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0
+            ok = ok and self.reason_fn(self.h, ctypes.byref(why)) == 0
+            if ok:
+                self.rows.append((time.time(), float(mhz.value), int(why.value)))
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag.set()
+        self.thread.join(timeout=2)
+        self.nv.nvmlShutdown()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for r in self.rows if t0 <= r[0] <= t1]
+        note = f"NVML every {1e3 * self.period:.0f} ms, samples inside the timed region ({1e3 * (t1 - t0):.1f} ms)"
+        if not inside:
+            inside = self.rows
+            note = "NVML: no sample inside the timed region; all samples of the run"
+        reasons = sorted({name for r in inside for bit, name in self.REASONS.items() if r[2] & bit})
+        sm = [r[1] for r in inside]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms (used when NVML cannot be loaded)."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -208,6 +261,14 @@ class ClockSampler:
         reasons = sorted({names[i] for r in inside if len(r) > 8 for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def clock_sampler(gpu_id: str):
+    """The NVML sampler when the driver's NVML library loads, else nvidia-smi."""
+    try:
+        return NvmlClockSampler(gpu_id)
+    except Exception:
+        return ClockSampler(gpu_id)
 
 
 def gpu_id_for_smi(torch, dev: int) -> str:
@@ -509,7 +570,7 @@ def run_ours(args, rank: int, world: int, local: int):
     K = args.steps
     ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
           for n, _ in calls}
-    sampler = ClockSampler(gpu_id_for_smi(torch, local))
+    sampler = clock_sampler(gpu_id_for_smi(torch, local))
     sampler.start()
     time.sleep(0.4)
     barrier(world, dev)
@@ -885,6 +946,73 @@ def run_dbo_layers(args, dev, layers: int = 4, busy_fmas: int = 256) -> dict:
             "l2": "flushed before every run of the layers"}
 
 
+def run_dbo_layers_gemm(args, dev, layers: int = 2, reps: int = 5) -> dict:
+    """The [DBO] layer schedule on the 8192-token workload with the grouped bf16 GEMM as the MLP (random
+    bf16 weights, 26 GB, shared by the layers; A0 and S stand-ins without busy work): two streams against
+    the same work on one stream, with the GEMM on every SM or capped to leave SMs to the comm stream.
+    hidden_comm_fraction = (one stream - two streams) / (the dispatch and combine kernels alone)."""
+    import torch
+    import combine_router_top_gb300 as M
+    w = W.WORKLOADS["dbo"]
+    T1 = w.T - w.T // 2
+    pf = M.problem(w.T, w.H, w.E, w.k, w.R, w.C)
+    x = torch.from_numpy(x_of(w).view(np.int16)).to(dev)
+    lg = torch.from_numpy(np.stack([W.make_logits(w.with_(seed=w.seed + 31 * l)) for l in range(layers)])).to(dev)
+    s = torch.from_numpy(W.expert_scale(w)).to(dev)
+    wb = W.make_weights_bf16_device(w, dev)
+    bufs = [M.alloc_buffers(M.problem(T1, w.H, w.E, w.k, w.R, w.C), dev) for _ in range(2)]
+    h, shared, out = (torch.empty((w.T, w.H), dtype=torch.int16, device=dev) for _ in range(3))
+    comp, comm = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ctx = M.dbo_create()
+
+    def timed(launch):
+        ts = []
+        with torch.cuda.stream(comp):
+            for i in range(2 + reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(comp)
+                launch()
+                e1.record(comp)
+                e1.synchronize()
+                if i >= 2:
+                    ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    comp.wait_stream(torch.cuda.current_stream())
+    res = {}
+    for cap in [0, 128]:
+        a = M.dbo_layers_args(pf, layers, x, lg, s, bufs, h, shared, out, 0.75, 1.5, 0, expert_w=wb,
+                              mlp_max_blocks=cap)
+        res[cap] = (timed(lambda: M.dbo_layers(ctx, a, comp, comm)), timed(lambda: M.dbo_layers(ctx, a, comp, comp)))
+    a = M.dbo_layers_args(pf, layers, x, lg, s, bufs, h, shared, out, 0.75, 1.5, 0, expert_w=wb)
+    M.dbo_layers_capture(ctx, a, comp, comm)
+    graph = timed(lambda: M.dbo_graph_launch(ctx, comp))
+    ctx.close()
+    # the comm kernels alone, on the buffers the last run left (per layer: D and C of both micro-batches)
+    pu = [M.problem(w.T // 2, w.H, w.E, w.k, w.R, w.C), M.problem(T1, w.H, w.E, w.k, w.R, w.C)]
+    rows0 = [0, w.T // 2]
+
+    def comm_only():
+        for _ in range(layers):
+            for u in range(2):
+                b = bufs[u]
+                M.moe_dispatch(pu[u], h[rows0[u]:], b["topk_idx"], b["slot"], b["recv"], None, b["recv_src"], comp)
+                M.moe_combine(pu[u], b["y"], b["topk_idx"], b["topk_w"], b["slot"], out[rows0[u]:], comp)
+    comm_ms = timed(comm_only)
+    best_cap = min(res, key=lambda c: res[c][0])
+    two, one = res[best_cap]
+    return {"workload": f"dbo layers, grouped bf16 GEMM as the MLP: {layers} layers, T={w.T} split "
+                        f"{w.T // 2}/{T1}, H={w.H}, E={w.E}, top_k={w.k}, C={w.C}, bf16 rows and weights",
+            "ms_per_layer_two_streams": two / layers, "ms_per_layer_one_stream": one / layers,
+            "ms_per_layer_graph": graph / layers, "speedup_vs_one_stream": one / two,
+            "mlp_max_blocks": best_cap,
+            "by_mlp_cap": {str(c): {"two_streams_ms_per_layer": t / layers, "one_stream_ms_per_layer": o / layers}
+                           for c, (t, o) in res.items()},
+            "comm_kernels_ms_per_layer": comm_ms / layers,
+            "hidden_comm_fraction": max(0.0, (one - two) / comm_ms) if comm_ms > 0 else None,
+            "l2": "not flushed: 26 GB of weights stream through every layer"}
+
+
 def run_gemm(args, dev, reps: int = 10, experts: int = 0) -> dict:
     """The grouped fp8 GEMM on the tensor cores, fed by route + dispatch, at the
     DeepSeek-V3 decode shape (weight-streaming, bound by HBM) and at an
@@ -1040,6 +1168,7 @@ def main():
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--gemm-only", action="store_true", help="only the grouped GEMM measurement")
     ap.add_argument("--gemm-experts", type=int, default=0, help="with --gemm-only: E experts (profiling case)")
+    ap.add_argument("--dbo-only", action="store_true", help="only the dual-batch-overlap measurements")
     ap.add_argument("--all-configs", action="store_true",
                     help="only the per-configuration timings of route, dispatch, expert and combine")
     args = ap.parse_args()
@@ -1063,11 +1192,20 @@ def main():
         torch.cuda.set_device(dev)
         print(json.dumps({"expert_gemm": run_gemm(args, dev, experts=args.gemm_experts)}), flush=True)
         return
+    if args.dbo_only:
+        import torch
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"dbo": run_dbo(args, dev), "dbo_layers": run_dbo_layers(args, dev),
+                          "dbo_layers_gemm": run_dbo_layers_gemm(args, dev)}), flush=True)
+        return
     line, dev = run_ours(args, rank, world, local)
     if rank == 0:
         if world == 1 and not args.no_dbo:
             line["dbo"] = run_dbo(args, dev)
             line["dbo_layers"] = run_dbo_layers(args, dev)
+            if not args.no_gemm:
+                line["dbo_layers_gemm"] = run_dbo_layers_gemm(args, dev)
         if world == 1 and not args.no_gemm:
             line["expert_gemm"] = run_gemm(args, dev)
         if world == 1 and not args.no_cpu_baseline:

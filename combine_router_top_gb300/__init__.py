@@ -47,7 +47,8 @@ class moe_dbo_timing(C.Structure):
 class moe_dbo_layers_args(C.Structure):
     _fields_ = [("full", moe_problem), ("n_layers", C.c_int32), ("busy_fmas", C.c_int32), ("alpha", C.c_float),
                 ("sigma", C.c_float), ("x", C.c_void_p), ("logits", C.c_void_p), ("s", C.c_void_p),
-                ("bufs", moe_ubatch_bufs * 2), ("h", C.c_void_p), ("shared", C.c_void_p), ("out", C.c_void_p)]
+                ("bufs", moe_ubatch_bufs * 2), ("h", C.c_void_p), ("shared", C.c_void_p), ("out", C.c_void_p),
+                ("expert_w", C.c_void_p), ("mlp_max_blocks", C.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -355,14 +356,17 @@ def moe_layer_stand_in(x, out, a: float, busy_fmas: int = 0, stream=None):
                                                           _stream(stream)))
 
 
-def dbo_layers_args(p_full, n_layers, x, logits, s, bufs2, h, shared, out, alpha=1.0, sigma=1.0, busy_fmas=0):
-    """moe_dbo_layers_args from tensors (the struct keeps raw pointers: keep the tensors alive)."""
+def dbo_layers_args(p_full, n_layers, x, logits, s, bufs2, h, shared, out, alpha=1.0, sigma=1.0, busy_fmas=0,
+                    expert_w=None, mlp_max_blocks=0):
+    """moe_dbo_layers_args from tensors (the struct keeps raw pointers: keep the tensors alive).
+    expert_w: [E][H][H] bf16 weights for the grouped GEMM as the MLP, or None for the synthetic expert."""
     a = moe_dbo_layers_args()
     a.full = p_full
     a.n_layers, a.busy_fmas, a.alpha, a.sigma = int(n_layers), int(busy_fmas), float(alpha), float(sigma)
     a.x, a.logits, a.s = _ptr(x), _ptr(logits), _ptr(s)
     a.bufs[0], a.bufs[1] = ubatch_bufs(bufs2[0]), ubatch_bufs(bufs2[1])
     a.h, a.shared, a.out = _ptr(h), _ptr(shared), _ptr(out)
+    a.expert_w, a.mlp_max_blocks = _ptr(expert_w), int(mlp_max_blocks)
     return a
 
 

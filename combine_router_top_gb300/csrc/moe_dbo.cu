@@ -190,6 +190,8 @@ extern "C" int dbo_layers(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *
     if (a->n_layers < 1 || !a->s || !a->h || !a->shared || !a->out) return MOE_ERR_INVALID_ARG;
     if (d.dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;       // layer inputs are bf16 rows
     if (d.T > 0 && (!a->x || !a->logits)) return MOE_ERR_INVALID_ARG;
+    if (a->mlp_max_blocks < 0) return MOE_ERR_INVALID_ARG;
+    if (a->expert_w != nullptr && d.H % 64 != 0) return MOE_ERR_UNSUPPORTED;
 
     const int T0 = d.T / 2, T1 = d.T - T0;
     const int Tu[2] = {T0, T1}, row0[2] = {0, T0};
@@ -205,6 +207,7 @@ extern "C" int dbo_layers(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *
     moe_problem pc[2] = {p[0], p[1]};
     pc[0].max_blocks = pc[1].max_blocks = cap;
     moe_problem pe[2] = {p[0], p[1]};
+    if (a->expert_w != nullptr && a->mlp_max_blocks > 0) pe[0].max_blocks = pe[1].max_blocks = a->mlp_max_blocks;
     const int compute_cap = a->full.max_blocks;
 
     const size_t rowb = (size_t)d.H * 2;
@@ -246,7 +249,9 @@ extern "C" int dbo_layers(moe_dbo_ctx *ctx, const moe_dbo_layers_args *a, void *
     auto experts = [&](int u) -> int {                     // compute stream, after this micro-batch's dispatch
         const moe_ubatch_bufs &b = a->bufs[u];
         if (cudaStreamWaitEvent(cs, ctx->d[u], 0) != cudaSuccess) return MOE_ERR_CUDA;
-        const int r = moe_expert_synthetic(&pe[u], b.recv, b.recv_scale, b.counts, a->s, b.y, compute_stream);
+        const int r = a->expert_w != nullptr
+                          ? moe_expert_gemm_bf16(&pe[u], b.recv, b.counts, a->expert_w, b.y, compute_stream)
+                          : moe_expert_synthetic(&pe[u], b.recv, b.recv_scale, b.counts, a->s, b.y, compute_stream);
         if (r != MOE_OK) return r;
         return cudaEventRecord(ctx->mlp[u], cs) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     };

@@ -392,13 +392,19 @@ typedef struct moe_dbo_layers_args {
     void *h;                  /* [T][H] bf16 scratch: A0 output, dispatched rows      */
     void *shared;             /* [T][H] bf16: S output of the last layer             */
     void *out;                /* [T][H] bf16: layer activations; layer L's output    */
+    const void *expert_w;     /* NULL: MLP = moe_expert_synthetic with s; else [E][H][H] bf16
+                                 weights (output-major, shared by every layer): MLP =
+                                 moe_expert_gemm_bf16 (needs H % 64 == 0)               */
+    int32_t mlp_max_blocks;   /* with expert_w: at most this many CTAs for the GEMM (0: one
+                                 per SM), leaving SMs to the comm-stream kernels         */
 } moe_dbo_layers_args;
 
 /* L layers of the [DBO §Introduction] schedule on two streams of one GPU.
  * Per layer l and micro-batch u: A0 (h = bf16(x_u * alpha), x_u the layer's
  * input), A1 (moe_route on logits[l]), D (moe_dispatch of h), MLP
- * (moe_expert_synthetic), S (shared = bf16(h * sigma)) and C (moe_combine,
- * whose output is the next layer's input). A0, A1, MLP and S run on
+ * (moe_expert_synthetic, or the grouped bf16 GEMM with expert_w), S
+ * (shared = bf16(h * sigma)) and C (moe_combine, whose output is the next
+ * layer's input). A0, A1, MLP and S run on
  * `compute`, D and C on `comm`, enqueued in the page's order:
  *   D_1 | A0_0 A1_0 | D_0 | MLP_1 | C_1 | S_1 | MLP_0 | C_0 | S_0 | A0_1 A1_1 (next layer)
  * with each receive as an event wait; a prologue runs layer 0's A0_1 A1_1.

@@ -227,18 +227,21 @@ def combine(y: np.ndarray, topk_idx, topk_w, slot, T: int):
     return out
 
 
-def run_path(x, logits, s, k: int, R: int, Cap: int, fp8: bool) -> dict:
-    """Route -> count -> dispatch -> synthetic expert -> combine on one batch."""
+def run_path(x, logits, s, k: int, R: int, Cap: int, fp8: bool, expert_w=None) -> dict:
+    """Route -> count -> dispatch -> experts -> combine on one batch. The experts are the
+    synthetic stand-in y = x * s_e, or with expert_w ([E][H][H] bf16 bits, bf16 rows only)
+    the grouped GEMM y[e][r] = bf16(sum_i x_i w[e][n][i])."""
     T, E = logits.shape
     idx, w = route(logits, k)
     c = count(idx, E, R, Cap)
     if fp8:
+        assert expert_w is None, "GEMM experts on fp8 rows take block-scaled weights: expert_gemm_fp8"
         rq, rs, src = dispatch_fp8(x, idx, c["slot"], E, Cap)
         y = expert_synthetic(rq, rs, c["counts"], s)
         res = {"recv_q": rq, "recv_scale": rs}
     else:
         rx, src = dispatch_bf16(x, idx, c["slot"], E, Cap)
-        y = expert_synthetic(rx, None, c["counts"], s)
+        y = expert_synthetic(rx, None, c["counts"], s) if expert_w is None else expert_gemm_bf16(rx, c["counts"], expert_w)
         res = {"recv_x": rx}
     out = combine(y, idx, w, c["slot"], T)
     res.update(c)
@@ -279,12 +282,14 @@ def scale_rows(x: np.ndarray, a: float) -> np.ndarray:
     return out
 
 
-def run_dbo_layers(x, logits_layers, s, k: int, R: int, Cap: int, alpha: float, sigma: float) -> dict:
+def run_dbo_layers(x, logits_layers, s, k: int, R: int, Cap: int, alpha: float, sigma: float,
+                   expert_w=None) -> dict:
     """Layers of the dual-batch-overlap schedule, micro-batch by micro-batch.
     [DBO §Introduction]: per layer and micro-batch u, A0 (here h = bf16(x a)),
-    A1 (the MoE gate: route on the layer's logits), dispatch of h, the experts,
-    S (shared expert: bf16(h s)) and combine, whose output is the next layer's
-    input. Returns the last layer's output and shared-expert output."""
+    A1 (the MoE gate: route on the layer's logits), dispatch of h, the experts
+    (the synthetic stand-in, or the grouped GEMM with expert_w), S (shared
+    expert: bf16(h s)) and combine, whose output is the next layer's input.
+    Returns the last layer's output and shared-expert output."""
     L, T, E = logits_layers.shape
     H = x.shape[1]
     out = np.empty((T, H), dtype=np.uint16)
@@ -295,7 +300,7 @@ def run_dbo_layers(x, logits_layers, s, k: int, R: int, Cap: int, alpha: float, 
         xu = np.ascontiguousarray(x[a:b])
         for l in range(L):
             h = scale_rows(xu, alpha)
-            r = run_path(h, logits_layers[l, a:b], s, k, R, Cap, False)
+            r = run_path(h, logits_layers[l, a:b], s, k, R, Cap, False, expert_w)
             shared[a:b] = scale_rows(h, sigma)
             xu = r["out"]
         out[a:b] = xu

@@ -579,6 +579,68 @@ def test_dbo_layers_full_size_as_benchmarked():
     ctx.close()
 
 
+def test_dbo_layers_with_gemm_experts():
+    """[DBO §Introduction] schedule with the grouped bf16 GEMM as the MLP (random bf16 weights, shared by
+    the layers): two streams give bit for bit what one stream gives; the GEMM grid capped to leave SMs to
+    the comm stream gives the same bits; and one layer is within the GEMM's bound of the oracle's
+    composition (A0 is exact and the routing identical, so out differs only through y):
+        |out - out_oracle| <= sum_j w_j (2^-11 S_j + ulp(y_oracle_j)) + 2 ulp(out_oracle),
+    S_j = sum_i |x_i w[e_j][n][i]|, the GEMM's bar for row j (see the GEMM tests)."""
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev, to_host
+    w = W.Workload("dbo_gemm", T=150, H=512, E=16, k=4, R=4, C=96, seed=808)
+    alpha, sigma = 0.75, 1.5
+    wb = W.make_weights_bf16(w)
+    wd = to_dev(wb)
+    results = {}
+    for L in [1, 2]:
+        x, lg, s, t, bufs, args = _layers_setup(w, L, alpha, sigma, 0)
+        comp, comm = torch.cuda.Stream(), torch.cuda.Stream()
+        comp.wait_stream(torch.cuda.current_stream())
+        ctx = M.dbo_create()
+        for mode, (streams, cap) in {"two": ((comp, comm), 0), "one": ((comp, comp), 0),
+                                     "two_capped": ((comp, comm), 100)}.items():
+            a = M.dbo_layers_args(args.full, L, t["x"], t["lg"], t["s"], bufs, t["h"], t["shared"], t["out"], alpha,
+                                  sigma, 0, expert_w=wd, mlp_max_blocks=cap)
+            t["out"].fill_(0)
+            torch.cuda.synchronize()
+            M.dbo_layers(ctx, a, *streams)
+            torch.cuda.synchronize()
+            results[(L, mode)] = to_host(t["out"], np.uint16).copy()
+        ctx.close()
+        assert np.array_equal(results[(L, "two")], results[(L, "one")])
+        assert np.array_equal(results[(L, "two")], results[(L, "two_capped")])
+        if L == 1:
+            got = results[(1, "two")]
+
+            def f64(bits):
+                return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+            def ulp(v):
+                a = np.abs(v)
+                return np.where(a > 0, 2.0 ** (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 7), 2.0 ** -133)
+            absw = np.abs(f64(wb))                                   # [E][H][H]
+            bound = np.zeros((w.T, w.H))
+            o = O.run_dbo_layers(x, lg, s, w.k, w.R, w.C, alpha, sigma, expert_w=wb)
+            for (a0, a1) in [(0, w.T // 2), (w.T // 2, w.T)]:
+                h = O.scale_rows(np.ascontiguousarray(x[a0:a1]), alpha)
+                r = O.run_path(h, lg[0, a0:a1], s, w.k, w.R, w.C, False, wb)
+                assert np.array_equal(r["out"], o["out"][a0:a1])
+                habs = np.abs(f64(h))
+                for tt in range(a1 - a0):
+                    for j in range(w.k):
+                        sl = r["slot"][tt, j]
+                        if sl < 0:
+                            continue
+                        e = r["topk_idx"][tt, j]
+                        S = absw[e] @ habs[tt]
+                        bound[a0 + tt] += r["topk_w"][tt, j] * (2.0 ** -11 * S + ulp(f64(r["y"][e, sl])))
+            oo = f64(o["out"])
+            err = np.abs(f64(got) - oo)
+            assert np.all(err <= bound + 2 * ulp(oo)), f"max excess {np.max(err - bound - 2 * ulp(oo))}"
+
+
 @pytest.mark.parametrize("name", ["tiny", "dsv3_fp8"])
 def test_path_host_equals_the_device_path(name):
     """moe_path_host (host x and logits in, host out, one call per batch),
