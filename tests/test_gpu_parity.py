@@ -584,7 +584,7 @@ def test_dbo_layers_with_gemm_experts():
     the layers): two streams give bit for bit what one stream gives; the GEMM grid capped to leave SMs to
     the comm stream gives the same bits; and one layer is within the GEMM's bound of the oracle's
     composition (A0 is exact and the routing identical, so out differs only through y):
-        |out - out_oracle| <= sum_j w_j (2^-11 S_j + ulp(y_oracle_j)) + 2 ulp(out_oracle),
+        |out - out_oracle| <= sum_j w_j ((K/8) 2^-24 S_j + ulp(y_oracle_j)) + 2 ulp(out_oracle),
     S_j = sum_i |x_i w[e_j][n][i]|, the GEMM's bar for row j (see the GEMM tests)."""
     import torch
     import combine_router_top_gb300 as M
@@ -635,7 +635,7 @@ def test_dbo_layers_with_gemm_experts():
                             continue
                         e = r["topk_idx"][tt, j]
                         S = absw[e] @ habs[tt]
-                        bound[a0 + tt] += r["topk_w"][tt, j] * (2.0 ** -11 * S + ulp(f64(r["y"][e, sl])))
+                        bound[a0 + tt] += r["topk_w"][tt, j] * ((w.H / 8) * 2.0 ** -24 * S + ulp(f64(r["y"][e, sl])))
             oo = f64(o["out"])
             err = np.abs(f64(got) - oo)
             assert np.all(err <= bound + 2 * ulp(oo)), f"max excess {np.max(err - bound - 2 * ulp(oo))}"
