@@ -28,7 +28,7 @@ MOE_DTYPE_FP8_E4M3_B128 = 1
 
 class moe_problem(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("num_tokens", "hidden", "num_experts", "top_k", "num_ranks",
-                                         "capacity", "dispatch_dtype", "max_blocks")]
+                                         "capacity", "dispatch_dtype", "max_blocks", "tokens_per_src_rank")]
 
 
 class moe_ubatch_bufs(C.Structure):
@@ -77,6 +77,7 @@ def lib() -> C.CDLL:
             "moe_route": ([pp, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
             "moe_route_noalloc": ([pp, P, P, P, P, P, P, P, P, P], i),
             "moe_dispatch": ([pp, P, P, P, P, P, P, P], i),
+            "moe_src_offsets": ([pp, P, P, P, P], i),
             "moe_route_dispatch_workspace_bytes": ([pp], C.c_size_t),
             "moe_route_dispatch": ([pp, P, P, P, P, P, P, P, P, P, P, P, P, P, C.c_size_t, P], i),
             "moe_expert_synthetic": ([pp, P, P, P, P, P, P], i),
@@ -103,7 +104,7 @@ def lib() -> C.CDLL:
 
 
 EXPORTS = ("moe_status_string", "moe_validate", "moe_device_status", "moe_route_workspace_bytes", "moe_route", "moe_route_noalloc",
-           "moe_dispatch", "moe_route_dispatch_workspace_bytes", "moe_route_dispatch",
+           "moe_dispatch", "moe_src_offsets", "moe_route_dispatch_workspace_bytes", "moe_route_dispatch",
            "moe_expert_synthetic", "moe_expert_gemm_fp8", "moe_expert_gemm_bf16", "moe_ready_flags_bytes", "moe_expert_combine", "moe_path_host",
            "moe_combine", "dbo_create", "dbo_destroy", "dbo_step", "dbo_read_timing",
            "moe_layer_stand_in", "dbo_layers", "dbo_layers_capture", "dbo_graph_launch")
@@ -113,8 +114,8 @@ def moe_status_string(status: int) -> str:
     return lib().moe_status_string(status).decode()
 
 
-def problem(T, H, E, k, R, Cap, dtype=MOE_DTYPE_BF16, max_blocks=0) -> moe_problem:
-    return moe_problem(T, H, E, k, R, Cap, dtype, max_blocks)
+def problem(T, H, E, k, R, Cap, dtype=MOE_DTYPE_BF16, max_blocks=0, tokens_per_src_rank=0) -> moe_problem:
+    return moe_problem(T, H, E, k, R, Cap, dtype, max_blocks, tokens_per_src_rank)
 
 
 def _ptr(t):
@@ -167,6 +168,18 @@ def moe_route_noalloc(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_c
     rc = lib().moe_route_noalloc(C.byref(p), _ptr(logits), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
                                  _ptr(offsets), _ptr(slot), _ptr(rank_counts), _ptr(dropped), _stream(stream))
     _check("moe_route_noalloc", rc)
+
+
+def src_ranks(p) -> int:
+    """S, the number of virtual data-parallel source ranks of problem p."""
+    T, tps = p.num_tokens, p.tokens_per_src_rank
+    return max(1, (T + tps - 1) // tps) if tps > 0 else 1
+
+
+def moe_src_offsets(p, counts, recv_src, src_offsets, stream=None):
+    """src_offsets [E][S+1]: per expert, the first row of each source rank's tokens."""
+    rc = lib().moe_src_offsets(C.byref(p), _ptr(counts), _ptr(recv_src), _ptr(src_offsets), _stream(stream))
+    _check("moe_src_offsets", rc)
 
 
 def moe_dispatch(p, x, topk_idx, slot, recv, recv_scale, recv_src, stream=None):

@@ -56,7 +56,7 @@ int check_problem(const moe_problem *p, Dims *d) {
     if (p->dispatch_dtype != MOE_DTYPE_BF16 && p->dispatch_dtype != MOE_DTYPE_FP8_E4M3_B128)
         return MOE_ERR_INVALID_ARG;
     if (p->dispatch_dtype == MOE_DTYPE_FP8_E4M3_B128 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
-    if (p->max_blocks < 0) return MOE_ERR_INVALID_ARG;
+    if (p->max_blocks < 0 || p->tokens_per_src_rank < 0) return MOE_ERR_INVALID_ARG;
     if (T * k >= (1LL << 31) || E * C >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
     if (d) {
         d->T = (int)T; d->H = (int)H; d->E = (int)E; d->k = (int)k;

@@ -581,3 +581,47 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
+
+// ---- per-source-rank row offsets inside each expert ---------------------------
+//
+// Rows of expert e are ordered by token, so by source rank: for every s the
+// first row whose token comes from source s or later is a lower bound over
+// recv_src. One block per expert, one thread per source rank (looping), each
+// a binary search over the expert's kept rows.
+namespace moe {
+namespace {
+__global__ void __launch_bounds__(256)
+src_offsets_kernel(const int32_t *__restrict__ counts, const int32_t *__restrict__ recv_src, int32_t *__restrict__ out,
+                   int C, int tps, int S) {
+    pdl_enter();
+    const int e = blockIdx.x;
+    const int kept = min(__ldg(counts + e), C);
+    const int32_t *src = recv_src + (size_t)e * C;
+    for (int s = threadIdx.x; s <= S; s += blockDim.x) {
+        int lo = 0, hi = kept;                              // first row with src[row] / tps >= s
+        const long long first_token = (long long)s * tps;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((long long)__ldg(src + mid) < first_token) lo = mid + 1; else hi = mid;
+        }
+        out[(size_t)e * (S + 1) + s] = lo;
+    }
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_src_offsets(const moe_problem *p, const int32_t *counts, const int32_t *recv_src,
+                               int32_t *src_offsets, void *stream) {
+    using namespace moe;
+    Dims d;
+    const int rc = check_problem(p, &d);
+    if (rc != MOE_OK) return rc;
+    if (!counts || !recv_src || !src_offsets) return MOE_ERR_INVALID_ARG;
+    if (!aligned(counts, 4) || !aligned(recv_src, 4) || !aligned(src_offsets, 4)) return MOE_ERR_INVALID_ARG;
+    const int tps = p->tokens_per_src_rank > 0 ? p->tokens_per_src_rank : (d.T > 0 ? d.T : 1);
+    const int S = d.T > 0 ? (int)(((long long)d.T + tps - 1) / tps) : 1;
+    if (launch_pdl(src_offsets_kernel, d.E, 256, as_stream(stream), counts, recv_src, src_offsets, d.C, tps, S) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}

@@ -85,6 +85,12 @@ typedef struct moe_problem {
                                 thread blocks for dispatch / expert / combine and
                                 the persistent GEMM and readiness grids, so that
                                 kernels on another stream stay co-resident */
+    int32_t tokens_per_src_rank; /* tokens each virtual data-parallel source rank
+                                contributes: token t comes from source rank
+                                t / tokens_per_src_rank, S = max(1, ceil(T /
+                                tokens_per_src_rank)) ranks (the last may hold
+                                fewer); 0 means one source rank of all T tokens.
+                                Used by moe_src_offsets only. */
 } moe_problem;
 
 /* Human-readable name of a moe_status value. Never NULL; static storage. */
@@ -186,6 +192,23 @@ int moe_route_noalloc(const moe_problem *p, const float *logits,
 int moe_dispatch(const moe_problem *p, const void *x,
                  const int32_t *topk_idx, const int32_t *slot,
                  void *recv, float *recv_scale, int32_t *recv_src, void *stream);
+
+/* Where each source rank's tokens sit inside each expert's rows.
+ * [PMC §Dispatch]: the receiver unpacks the tokens into one tensor for the
+ * grouped GEMM, all tokens of one expert grouped together across the
+ * data-parallel ranks that sent them. Here a token's slot ascends with its
+ * index, so the kept rows of expert e are ordered by source rank
+ * s(t) = t / tokens_per_src_rank, and
+ *   src_offsets[e][s] = number of kept rows of expert e whose token comes from
+ *                       a source rank below s,   s = 0 .. S,
+ * so rows [src_offsets[e][s], src_offsets[e][s+1]) of expert e came from
+ * source rank s, and src_offsets[e][S] = min(counts[e], C).
+ * counts and recv_src are moe_route's and moe_dispatch's outputs for the same
+ * problem. src_offsets: device i32[E][S+1] (S from tokens_per_src_rank; S = 1
+ * when it is 0). One block per expert; a programmatic dependent of the
+ * previous kernel. */
+int moe_src_offsets(const moe_problem *p, const int32_t *counts, const int32_t *recv_src,
+                    int32_t *src_offsets, void *stream);
 
 /* moe_route followed by moe_dispatch in one call, with the same outputs bit
  * for bit, for decode: [PMC §Dispatch] counts tokens per destination inside

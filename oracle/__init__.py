@@ -42,6 +42,7 @@ def lib():
             "oracle_dispatch_fp8": [i32, i32, i32, i32, i32, P, P, P, P, P, P],
             "oracle_expert_synthetic": [i32, i32, i32, i32, P, P, P, P, P],
             "oracle_combine": [i32, i32, i32, i32, i32, P, P, P, P, P],
+            "oracle_src_offsets": [i32, i32, i32, i32, P, P, P],
             "oracle_scale_rows": [i64, P, C.c_float, P],
             "oracle_gemm_fp8_row": [i32, i32, P, P, P, P, P],
             "oracle_expert_gemm_fp8": [i32, i32, i32, i32, P, P, P, P, P, P],
@@ -149,6 +150,18 @@ def dispatch_fp8(x: np.ndarray, topk_idx, slot, E: int, Cap: int):
                                      _p(np.ascontiguousarray(slot, dtype=np.int32)), _p(recv_q), _p(recv_scale),
                                      _p(recv_src)), "oracle_dispatch_fp8")
     return recv_q, recv_scale, recv_src
+
+
+def src_offsets(topk_idx, slot, E: int, tokens_per_src_rank: int):
+    """[E][S+1]: per expert, the number of kept pairs from source ranks below s (s = 0 .. S)."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = idx.shape
+    tps = int(tokens_per_src_rank)
+    S = max(1, -(-T // tps)) if tps > 0 else 1
+    out = np.empty((E, S + 1), dtype=np.int32)
+    _check(lib().oracle_src_offsets(T, E, k, tps, _p(idx), _p(np.ascontiguousarray(slot, dtype=np.int32)), _p(out)),
+           "oracle_src_offsets")
+    return out
 
 
 def expert_synthetic(recv, recv_scale, counts, s):

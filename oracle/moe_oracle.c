@@ -349,6 +349,37 @@ int oracle_dispatch_fp8(int32_t T, int32_t H, int32_t E, int32_t k, int32_t C,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Source-rank offsets inside each expert. [PMC §Dispatch]: the receiver     */
+/* groups all tokens of one expert together across the data-parallel ranks  */
+/* that sent them. Token t comes from source rank t / tps (tps tokens per    */
+/* rank; tps = 0: one rank), S = max(1, ceil(T / tps)). For s = 0 .. S:      */
+/*   src_offsets[e][s] = number of kept pairs (t, j) with topk_idx = e and   */
+/*                       source rank of t below s,                           */
+/* counted over the pairs, so it does not depend on where dispatch put them. */
+/* ------------------------------------------------------------------------ */
+int oracle_src_offsets(int32_t T, int32_t E, int32_t k, int32_t tps, const int32_t *topk_idx,
+                       const int32_t *slot, int32_t *src_offsets)
+{
+    if (T < 0 || E < 1 || k < 1 || tps < 0)
+        return -1;
+    const int32_t per = tps > 0 ? tps : (T > 0 ? T : 1);
+    const int32_t S = T > 0 ? (int32_t)(((int64_t)T + per - 1) / per) : 1;
+    memset(src_offsets, 0, sizeof(int32_t) * (size_t)E * (size_t)(S + 1));
+    for (int32_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < k; ++j) {
+            if (slot[(int64_t)t * k + j] < 0)
+                continue;
+            const int32_t e = topk_idx[(int64_t)t * k + j];
+            src_offsets[(int64_t)e * (S + 1) + t / per + 1] += 1;    /* counted at every s above t's rank */
+        }
+    }
+    for (int32_t e = 0; e < E; ++e)
+        for (int32_t s = 1; s <= S; ++s)
+            src_offsets[(int64_t)e * (S + 1) + s] += src_offsets[(int64_t)e * (S + 1) + s - 1];
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Synthetic expert (stands in for the grouped GEMM of [PMC §Dispatch]):     */
 /*   bf16 input:  y = bf16(float(x) * s_e)                                   */
 /*   fp8 input:   y = bf16((float(q) * scale) * s_e)                         */

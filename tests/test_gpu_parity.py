@@ -721,3 +721,28 @@ def test_fp32_order_cases_by_hand():
                            to_dev(np.array([0, 1], np.int32)), to_dev(s), yd)
     torch.cuda.synchronize()
     assert np.all(to_host(yd, np.uint16)[1, 0] == int(c["y_bf16_bits"], 16))
+
+
+@pytest.mark.parametrize("name,T,tps,Cap", [("dsv3_fp8", 1024, 128, 128), ("v2lite", 256, 0, 256),
+                                           ("mixtral_skew", 1000, 512, 200), ("dsv3_fp8", 77, 10, 4),
+                                           ("dsv3_fp8", 0, 128, 128)])
+def test_src_offsets_match_the_oracle(name, T, tps, Cap):
+    """moe_src_offsets on the GPU's own route and dispatch output: bit for bit the oracle's offsets,
+    which it counts over the pairs (ragged last source rank, drops and an empty batch included)."""
+    import torch
+    import combine_router_top_gb300 as M
+    from gpu_path import to_dev, to_host
+    w = W.WORKLOADS[name].with_(T=T, C=Cap) if T > 0 else W.WORKLOADS[name].with_(T=1, C=Cap)
+    x, lg = W.make_x(w), W.make_logits(w)
+    x, lg = x[:T], lg[:T]
+    p = M.problem(T, w.H, w.E, w.k, w.R, Cap, w.dtype, 0, tps)
+    b = M.alloc_buffers(p, "cuda:0")
+    M.run_path(p, to_dev(np.ascontiguousarray(x)), to_dev(np.ascontiguousarray(lg)),
+               to_dev(W.expert_scale(w)), b, torch.empty((max(T, 1), w.H), dtype=torch.int16, device="cuda:0"))
+    S = M.src_ranks(p)
+    off = torch.full((w.E, S + 1), -5, dtype=torch.int32, device="cuda:0")
+    M.moe_src_offsets(p, b["counts"], b["recv_src"], off)
+    torch.cuda.synchronize()
+    idx, _ = O.route(np.ascontiguousarray(lg), w.k)
+    c = O.count(idx, w.E, w.R, Cap)
+    assert np.array_equal(to_host(off), O.src_offsets(idx, c["slot"], w.E, tps))

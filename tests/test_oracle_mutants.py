@@ -81,6 +81,12 @@ MUTANTS = {
     # fp8 expert: the two scales multiplied first
     "expert_fp8_scale_first": ("float deq = e4m3_decode(((const uint8_t *)recv)[row * H + h]) * recv_scale[row * nb + h / 128];\n                    v = deq * s[e];",
                                "float deq = e4m3_decode(((const uint8_t *)recv)[row * H + h]) * (recv_scale[row * nb + h / 128] * s[e]);\n                    v = deq;"),
+    # source offsets: dropped pairs counted too
+    "src_offsets_count_dropped": ("            if (slot[(int64_t)t * k + j] < 0)\n                continue;\n            const int32_t e = topk_idx",
+                                  "            const int32_t e = topk_idx"),
+    # source offsets: a pair counted at its own rank's entry instead of the ranks above it
+    "src_offsets_inclusive": ("src_offsets[(int64_t)e * (S + 1) + t / per + 1] += 1;",
+                              "src_offsets[(int64_t)e * (S + 1) + t / per] += 1;"),
     # gemm: the weight read transposed (w[k][n] instead of w[n][k]), kept in bounds
     "gemm_weight_transposed": ("block += (double)e4m3_decode(q_row[i]) * (double)e4m3_decode(wn[i]);",
                                "block += (double)e4m3_decode(q_row[i]) * (double)e4m3_decode(w[(int64_t)(i % N) * K + n % K]);"),

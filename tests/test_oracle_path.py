@@ -234,6 +234,33 @@ def test_dispatch_rows_grouped_by_source_rank(inputs_of):
         assert np.all(np.diff(t_of // per_src) >= 0)
 
 
+@pytest.mark.parametrize("name,tps", [("dsv3_fp8", 128), ("dsv3_fp8", 100), ("v2lite", 0), ("v2lite", 1),
+                                      ("mixtral_skew", 512)])
+def test_src_offsets_bound_each_source_ranks_rows(name, tps, inputs_of):
+    """[PMC §Dispatch] groups one expert's tokens across the DP ranks that sent them. The offsets,
+    counted over the pairs, must cut the dispatched rows (placed by the slots) at the source-rank
+    boundaries: numpy's searchsorted over recv_src // tps finds the same cuts; the last offset is the
+    expert's kept rows; per source, the rows over all experts are that source's kept pairs."""
+    w = W.WORKLOADS[name]
+    d = inputs_of(name)
+    T = w.T if name != "mixtral_skew" else 1000              # a partial last source rank too
+    r = O.run_path(d["x"][:T], d["logits"][:T], d["s"], w.k, w.R, min(w.C, 200), False)
+    Cap = min(w.C, 200)
+    off = O.src_offsets(r["topk_idx"], r["slot"], w.E, tps)
+    S = max(1, -(-T // tps)) if tps > 0 else 1
+    per = tps if tps > 0 else T
+    assert off.shape == (w.E, S + 1)
+    kept = np.minimum(r["counts"], Cap)
+    assert np.array_equal(off[:, 0], np.zeros(w.E)) and np.array_equal(off[:, S], kept)
+    for e in range(w.E):
+        src_rank = r["recv_src"][e, :kept[e]] // per
+        assert np.all(np.diff(src_rank) >= 0)
+        assert np.array_equal(off[e], np.searchsorted(src_rank, np.arange(S + 1), side="left"))
+    for s_ in range(S):
+        rows = int(np.sum(off[:, s_ + 1] - off[:, s_]))
+        assert rows == int(np.sum(r["slot"][s_ * per:(s_ + 1) * per] >= 0))
+
+
 def test_dispatch_fp8_against_torch_and_bounds(inputs_of):
     w = W.WORKLOADS["dsv3_fp8"]
     d = inputs_of("dsv3_fp8")
