@@ -211,9 +211,11 @@ dispatch_fp8_seg_kernel(const uint16_t *__restrict__ x, const int32_t *__restric
     pdl_enter();
     const int tid = threadIdx.x, lane = tid & 31;
     const int segs = H / kFp8Seg, nb = H / 128;
-    const long long units = (long long)T * segs;
-    for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-        const int t = (int)(u / segs), seg = (int)(u % segs);
+    // T * segs <= 2^24 * 64 = 2^30: unit indices and their split stay in 32 bits
+    const unsigned units = (unsigned)T * (unsigned)segs;
+    for (unsigned u = blockIdx.x; u < units; u += gridDim.x) {
+        const unsigned t32 = u / (unsigned)segs;
+        const int t = (int)t32, seg = (int)(u - t32 * (unsigned)segs);
         // the 16 elements of task tid: two 16-byte loads, coalesced across the CTA
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H + (size_t)seg * kFp8Seg) + 2 * tid;
         const uint4 a = ld_stream_v4(src), c = ld_stream_v4(src + 1);
