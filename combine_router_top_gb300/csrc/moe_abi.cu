@@ -110,7 +110,7 @@ size_t moe_route_workspace_bytes(const moe_problem *p) {
     moe::Dims d;
     if (moe::check_problem(p, &d) != MOE_OK) return 0;
     size_t bytes;
-    if (moe::route_small(d.T)) {
+    if (moe::route_small(d.T, d.E)) {
         bytes = (size_t)d.E * moe::route_small_stride(d.T);              // one byte per (expert, tile of 8)
     } else {
         const size_t tiles = ((size_t)d.T + moe::kTileTokens - 1) / moe::kTileTokens;

@@ -324,7 +324,7 @@ constexpr size_t fused_smem_bytes(int H, int E) {
 // FP8: quantise the staged row and store codes and scales; bf16: store the
 // staged row itself to each kept destination.
 template <bool FP8>
-__global__ void __launch_bounds__(kFusedThreads)
+__global__ void __launch_bounds__(kFusedThreads, 6)     // 6 blocks (40 registers a thread) per SM, as before the byte-count totals
 route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ topk_idx,
                           const uint8_t *__restrict__ cnt8, int stride,
                           int32_t *__restrict__ slot, uint8_t *__restrict__ recv_q, float *__restrict__ recv_scale,
@@ -342,7 +342,9 @@ route_dispatch_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict_
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (blockIdx.x == 0) {          // the totals block: first, so that it is no tail of the grid
         pdl_enter();
-        small_route_totals(cnt8, (size_t)stride, n_tiles, E, R, C, counts, offsets, rank_counts, dropped,
+        // (not on the critical path: it runs beside the token blocks; 4 loads a
+        // thread in flight keep it within the 40 registers of the token blocks)
+        small_route_totals<4>(cnt8, (size_t)stride, n_tiles, E, R, C, counts, offsets, rank_counts, dropped,
                            reinterpret_cast<int *>(fused_smem), s_wsum);
         return;
     }
@@ -545,7 +547,7 @@ extern "C" int moe_route_dispatch(const moe_problem *p, const float *logits, con
     if (workspace_bytes < moe_route_dispatch_workspace_bytes(p)) return MOE_ERR_INVALID_ARG;
     const bool fp8 = d.dtype == MOE_DTYPE_FP8_E4M3_B128;
     const int n_tiles = (d.T + kSmallTileTokens - 1) / kSmallTileTokens;
-    const bool fused = d.H <= kFusedMaxHidden && d.T <= kFusedMaxTokens && d.max_blocks == 0;
+    const bool fused = d.H <= kFusedMaxHidden && d.T <= kFusedMaxTokens && route_small(d.T, d.E) && d.max_blocks == 0;
     if (!fused) {
         rc = moe_route(p, logits, topk_idx, topk_w, counts, offsets, slot, rank_counts, dropped, workspace,
                        workspace_bytes, stream);

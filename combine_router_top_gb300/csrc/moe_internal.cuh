@@ -30,7 +30,15 @@ constexpr int kChunkTiles = 32;    // route tiles per chunk of the two-level sca
 // row e: at most 512 bytes, one 16-byte piece per lane of a warp.
 constexpr int kSmallTileTokens = 8;
 constexpr int kRouteSmallMaxTokens = 4096;
-inline bool route_small(long long T) { return T <= kRouteSmallMaxTokens; }
+// 16-byte pieces of the byte counts the totals block reads: E rows of
+// ceil(tiles / 16) pieces. The small-batch route runs while that is at most
+// 8 pieces per thread of the block (1024 tokens at E = 256, 4096 at E <= 64);
+// beyond, one block reading them is slower than the 32-token tiles.
+constexpr int kRouteSmallMaxPieces = 8 * 256;
+inline bool route_small(long long T, int E) {
+    const long long tiles = (T + kSmallTileTokens - 1) / kSmallTileTokens;
+    return T <= kRouteSmallMaxTokens && (long long)E * ((tiles + 15) / 16) <= kRouteSmallMaxPieces;
+}
 // Bytes per expert row of the small-batch workspace: the tile count rounded up to 16.
 inline size_t route_small_stride(long long T) {
     const size_t tiles = ((size_t)T + kSmallTileTokens - 1) / kSmallTileTokens;
@@ -452,22 +460,44 @@ __device__ __forceinline__ int warp_row_prefix(const uint8_t *__restrict__ row, 
 // One block (any multiple of 32 threads, at most 1024) turns the byte counts
 // cnt8[E][stride] of n_tiles tiles into the totals: counts[e], offsets[0..E]
 // (exclusive scan), rank_counts[r] (kept rows of the experts of rank r) and
-// dropped. tot: E ints, wsum: 32 ints, both shared.
+// dropped. tot: E ints, wsum: 32 ints, both shared. Each thread issues up to
+// BATCH loads before it uses any.
+template <int BATCH>
 __device__ inline void small_route_totals(const uint8_t *__restrict__ cnt8, size_t stride, int n_tiles, int E, int R,
                                           int C, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                                           int32_t *__restrict__ rank_counts, int32_t *__restrict__ dropped, int *tot,
                                           int *wsum) {
     const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int e = tid; e < E; e += nt) {
-        const uint8_t *row = cnt8 + (size_t)e * stride;
-        unsigned acc = 0;
-#pragma unroll 8
-        for (int c = 0; c < n_tiles; c += 16)
-            acc = add_bytes_below(__ldcg(reinterpret_cast<const uint4 *>(row + c)), c, n_tiles, acc);
-        tot[e] = (int)acc;
-        counts[e] = (int)acc;
+    // every (expert, 16-byte piece) pair is one load, spread over all threads
+    // (so that a few experts with long rows still use the whole block); the
+    // pieces of a row meet in an integer sum, whose order does not matter
+    const int pieces = (n_tiles + 15) / 16;
+    for (int e = tid; e < E; e += nt) tot[e] = 0;
+    __syncthreads();
+    const int pairs = E * pieces;
+    for (int base = 0; base < pairs; base += BATCH * nt) {  // one pass while pairs <= BATCH * threads
+        uint4 v[BATCH];
+        int ex[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {                  // all loads issued before any is used
+            const int i = base + j * nt + tid;
+            ex[j] = -1;
+            if (i < pairs) {
+                ex[j] = i / pieces;
+                v[j] = __ldcg(reinterpret_cast<const uint4 *>(cnt8 + (size_t)ex[j] * stride +
+                                                              (size_t)(i - ex[j] * pieces) * 16));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            if (ex[j] < 0) continue;
+            const int c = (base + j * nt + tid - ex[j] * pieces) * 16;
+            const unsigned sum = add_bytes_below(v[j], c, n_tiles, 0u);
+            if (sum != 0) atomicAdd(&tot[ex[j]], (int)sum);
+        }
     }
     __syncthreads();
+    for (int e = tid; e < E; e += nt) counts[e] = tot[e];
     // exclusive scan of tot over e: each thread a run of consecutive experts
     const int per = (E + nt - 1) / nt;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);

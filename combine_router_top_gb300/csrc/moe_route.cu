@@ -172,7 +172,7 @@ route_slots_small_kernel(int T, int n_tiles, int E, int k, int R, int C, const u
     __shared__ int wsum[32];
     pdl_enter();
     if (blockIdx.x == 0) {             // first, so that it is no tail of the grid
-        small_route_totals(cnt8, (size_t)stride, n_tiles, E, R, C, counts, offsets, rank_counts, dropped, tot, wsum);
+        small_route_totals<8>(cnt8, (size_t)stride, n_tiles, E, R, C, counts, offsets, rank_counts, dropped, tot, wsum);
         return;
     }
     const int lane = threadIdx.x & 31;
@@ -388,7 +388,7 @@ extern "C" int moe_route(const moe_problem *p, const float *logits, int32_t *top
         return MOE_ERR_INVALID_ARG;
 
     cudaStream_t st = as_stream(stream);
-    if (route_small(d.T)) {
+    if (route_small(d.T, d.E)) {
         // small batches: top-k per tile of 8 tokens, then slots and totals; the
         // second kernel is a programmatic dependent of the first
         uint8_t *cnt8 = static_cast<uint8_t *>(workspace);

@@ -110,13 +110,14 @@ int moe_device_status(void);
 int moe_validate(const moe_problem *p);
 
 /* Bytes of device workspace moe_route needs for this problem (host-only, no
- * CUDA call); 0 if the problem is invalid. Up to 4096 tokens the workspace
- * holds one byte per (expert, tile of 8 tokens), each expert's row rounded up
- * to 16 bytes: E * 16 * ceil(ceil(T/8) / 16) bytes. Beyond, it holds one
- * 32-bit count per (tile of 32 tokens, expert) and, for large batches (more
- * than 2^22 / E tiles squared), two 32-bit values per (chunk of 32 tiles,
- * expert) for a two-level scan of those counts. Always a multiple of 256 and
- * at least 256. Its contents need no initialisation. */
+ * CUDA call); 0 if the problem is invalid. For decode-sized batches (T <= 4096
+ * and E * ceil(ceil(T/8) / 16) <= 2048: 1024 tokens at E = 256, 4096 at
+ * E <= 64) the workspace holds one byte per (expert, tile of 8 tokens), each
+ * expert's row rounded up to 16 bytes: E * 16 * ceil(ceil(T/8) / 16) bytes.
+ * Otherwise it holds one 32-bit count per (tile of 32 tokens, expert) and, for
+ * large batches (more than 2^22 / E tiles squared), two 32-bit values per
+ * (chunk of 32 tiles, expert) for a two-level scan of those counts. Always a
+ * multiple of 256 and at least 256. Its contents need no initialisation. */
 size_t moe_route_workspace_bytes(const moe_problem *p);
 
 /* Step 1 and 2: router top-k with renormalised softmax weights, then the
@@ -212,8 +213,9 @@ int moe_src_offsets(const moe_problem *p, const int32_t *counts, const int32_t *
 
 /* moe_route followed by moe_dispatch in one call, with the same outputs bit
  * for bit, for decode: [PMC §Dispatch] counts tokens per destination inside
- * the dispatch kernel. For at most 1024 tokens, H <= 16384 and
- * max_blocks == 0 (fp8 or bf16 dispatch), it runs in two launches instead of
+ * the dispatch kernel. For at most 1024 tokens, H <= 16384, max_blocks == 0
+ * and a decode-sized route (see moe_route_workspace_bytes; every E <= 256 at
+ * 1024 tokens), for fp8 or bf16 dispatch, it runs in two launches instead of
  * three: the route's top-k kernel, then one kernel with a block per token
  * that forms the token's slots from the per-tile counts and dispatches its
  * row (launched as a programmatic dependent of the first). Otherwise it calls

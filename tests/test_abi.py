@@ -82,19 +82,22 @@ def test_validate_accepts_workloads(moe):
 
 
 def test_route_workspace_bytes(moe):
-    # up to 4096 tokens: one byte per (expert, tile of 8 tokens), each expert's row
-    # rounded up to 16 bytes: 1024 tokens -> 128 tiles, 256 experts
-    p = mk(moe)
-    assert moe.moe_route_workspace_bytes(p) == 256 * 128
-    assert moe.moe_route_workspace_bytes(mk(moe, T=4096)) == 256 * 512
-    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=500, k=5, R=4)) == (500 * 416 + 255) // 256 * 256
-    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=100, k=5, R=4)) == (100 * 416 + 255) // 256 * 256
+    # decode-sized batches (T <= 4096 and E * ceil(tiles8 / 16) <= 2048): one byte per
+    # (expert, tile of 8 tokens), each expert's row rounded up to 16 bytes
+    assert moe.moe_route_workspace_bytes(mk(moe)) == 256 * 128                  # 1024 tokens, E 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=4096, E=64, R=8)) == 64 * 512
+    assert moe.moe_route_workspace_bytes(mk(moe, T=4096, E=8, k=2, R=8)) == 8 * 512
     assert moe.moe_route_workspace_bytes(mk(moe, T=9, E=3, k=1, R=1)) == 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=256, E=1024, k=8, R=8)) == 1024 * 32
     # beyond: int32 counts per (tile of 32 tokens, expert); while tiles^2 * E <= 2^22
     # the finaliser sums earlier tiles directly, beyond that the two-level scan adds
     # a sum and a base per (chunk of 32 tiles, expert)
+    assert moe.moe_route_workspace_bytes(mk(moe, T=1025)) == 33 * 256 * 4        # 1025 tokens, E 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=4096)) == 128 * 256 * 4
     assert moe.moe_route_workspace_bytes(mk(moe, T=4097)) == (129 + 2 * 5) * 256 * 4
     assert moe.moe_route_workspace_bytes(mk(moe, T=4097, E=8, R=8)) == (129 * 8 * 4 + 255) // 256 * 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=500, k=5, R=4)) == ((102 + 2 * 4) * 500 * 4 + 255) // 256 * 256
+    assert moe.moe_route_workspace_bytes(mk(moe, T=3239, E=100, k=5, R=4)) == (102 * 100 * 4 + 255) // 256 * 256
     assert moe.moe_route_workspace_bytes(mk(moe, T=0)) == 256
     assert moe.moe_route_workspace_bytes(mk(moe, T=33, E=8, R=2)) % 256 == 0
 

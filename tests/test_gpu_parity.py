@@ -82,16 +82,20 @@ EDGE = {
     "H65536": W.Workload("H65536", T=3, H=65536, E=4, k=2, R=2, C=4, seed=12),
     "H65536_fp8": W.Workload("H65536f", T=5, H=65536, E=4, k=2, R=2, C=4, dtype=1, seed=19),
     "H128_fp8": W.Workload("H128", T=64, H=128, E=16, k=4, R=4, C=64, dtype=1, seed=13),
-    # up to 4096 tokens the route counts per tile of 8 tokens in bytes: E = 1024
-    # and E = 500 (more experts than threads in the totals block, not a
-    # multiple of 32), and the largest such batch
-    "T2049_E1024_small": W.Workload("t2049", T=2049, H=64, E=1024, k=6, R=8, C=64, seed=17),
-    "T3239_E500_small": W.Workload("t3239", T=3239, H=64, E=500, k=5, R=4, C=100, seed=18),
-    "T4096_E1024_k16_small_max": W.Workload("t4096", T=4096, H=64, E=1024, k=16, R=8, C=128, seed=20),
-    # beyond: tiles of 32 tokens; one token past the switch (129 tiles at
-    # E = 256: the two-level scan, a ragged last chunk), the direct sum of
-    # earlier tiles (256 tiles at E = 8), and the two-level scan at E = 1024
-    # and at E = 500 (two thread groups in the chunk scan)
+    # decode-sized batches count per tile of 8 tokens in bytes: E = 1024 (more
+    # experts than threads in the totals block, the most it takes: 256 tokens),
+    # E = 500 (not a multiple of 32) and the largest batch (4096 tokens at E 8)
+    "T256_E1024_k16_small": W.Workload("t256", T=256, H=64, E=1024, k=16, R=8, C=64, seed=20),
+    "T300_E500_small": W.Workload("t300", T=300, H=64, E=500, k=5, R=4, C=100, seed=18),
+    "T4096_E8_small_max": W.Workload("t4096", T=4096, H=64, E=8, k=2, R=2, C=4096, seed=25),
+    # beyond, tiles of 32 tokens: one token past the byte counts at E 256
+    # (33 tiles, direct sum), at E = 1024 (65 tiles: the two-level scan) and
+    # E = 500 (102 tiles, a ragged last chunk, two thread groups in the chunk scan)
+    "T1025_E256_direct": W.Workload("t1025", T=1025, H=64, E=256, k=8, R=8, C=128, seed=26),
+    "T2049_E1024_chunked": W.Workload("t2049", T=2049, H=64, E=1024, k=6, R=8, C=64, seed=17),
+    "T3239_E500_chunked": W.Workload("t3239", T=3239, H=64, E=500, k=5, R=4, C=100, seed=19),
+    # 129 tiles at E = 256 (two-level, ragged last chunk), the direct sum of
+    # earlier tiles (256 tiles at E = 8), and the two-level scan at 8193 and 5000 tokens
     "T4097_E256_chunked": W.Workload("t4097", T=4097, H=64, E=256, k=8, R=8, C=256, seed=21),
     "T8192_E8_direct": W.Workload("t8192", T=8192, H=64, E=8, k=2, R=2, C=4096, seed=22),
     "T8193_E1024_chunked": W.Workload("t8193", T=8193, H=64, E=1024, k=6, R=8, C=64, seed=23),
