@@ -1,4 +1,5 @@
-"""Host threads calling the library at once, from the very first call of a
+"""The library outside the usual single-threaded Python caller. Host threads
+calling the library at once, from the very first call of a
 process: the per-context host caches (device addresses of the library's
 arrays, shared-memory attributes, occupancy) are filled under concurrency,
 and every thread's results must equal a single-threaded run bit for bit.
@@ -69,3 +70,24 @@ def test_concurrent_first_calls_from_host_threads():
     r = subprocess.run([sys.executable, "-c", CHILD, ROOT], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
     assert "threads ok" in r.stdout
+
+
+def test_c_abi_from_plain_c():
+    """The C ABI from a plain C program (tests/c_abi_check.c): cudaMalloc'd buffers, route -> dispatch ->
+    synthetic expert -> combine for a bf16 and an fp8 batch, and the allocation-free route, each result
+    checked against the C oracle linked into the same program. No Python or PyTorch in that process."""
+    import shutil
+    import tempfile
+    from combine_router_top_gb300 import build as B
+    lib = B.build()
+    cuda = os.path.dirname(os.path.dirname(shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"))
+    libdir = os.path.dirname(lib)
+    exe = os.path.join(tempfile.mkdtemp(), "c_abi_check")
+    subprocess.run(["gcc", "-O2", "-std=c11", os.path.join(ROOT, "tests", "c_abi_check.c"),
+                    os.path.join(ROOT, "oracle", "moe_oracle.c"), "-I", os.path.join(ROOT, "include"),
+                    "-I", os.path.join(cuda, "include"), "-L", libdir, "-lmoe_gb300",
+                    "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm", "-Wl,-rpath," + libdir,
+                    "-Wl,-rpath," + os.path.join(cuda, "lib64"), "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    assert "c abi ok" in r.stdout
