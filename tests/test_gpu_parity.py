@@ -759,3 +759,36 @@ def test_src_offsets_match_the_oracle(name, T, tps, Cap):
     idx, _ = O.route(np.ascontiguousarray(lg), w.k)
     c = O.count(idx, w.E, w.R, Cap)
     assert np.array_equal(to_host(off), O.src_offsets(idx, c["slot"], w.E, tps))
+
+
+def _random_shapes(n, seed=2468):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        E = int(rng.choice([1, 2, 3, 6, 8, 16, 33, 64, 100, 256, 500, 1024]))
+        divisors = [r for r in range(1, E + 1) if E % r == 0]
+        R = int(rng.choice(divisors[:8]))
+        k = int(rng.integers(1, min(16, E) + 1))
+        fp8 = bool(rng.integers(0, 2))
+        H = int(rng.choice([128, 256, 1024, 2048, 3072])) if fp8 else int(rng.choice([8, 64, 200, 1024, 2056]))
+        T = int(rng.choice([1, 7, 31, 33, 100, 257, 1000, 1025, 2048, 3000]))
+        if T * E > 2_000_000 or T * H > 2_000_000:
+            continue
+        C = int(max(1, rng.integers(1, 2 * max(1, T * k // E) + 8)))
+        out.append(W.Workload(f"rnd{len(out)}", T=T, H=H, E=E, k=k, R=R, C=C, dtype=int(fp8),
+                              seed=int(rng.integers(0, 1 << 30))))
+    return out
+
+
+@pytest.mark.parametrize("w", _random_shapes(40), ids=lambda w: f"{w.name}-T{w.T}-H{w.H}-E{w.E}-k{w.k}-R{w.R}-C{w.C}-{'fp8' if w.dtype else 'bf16'}")
+def test_random_shapes_parity(w):
+    """Seeded random shapes (ragged token counts, 1 to 1024 experts, any k, capacities that drop pairs,
+    bf16 and fp8): both route paths (byte counts and 32-token tiles), every dispatch kernel, expert and
+    combine against the oracle at the usual bars; and the fused route + dispatch equals the separate calls."""
+    from gpu_path import compare, run_stages
+    g, o = run_both(w)
+    compare(g, o, w.C, w.dtype == W.DTYPE_FP8_E4M3_B128)
+    x, lg, s = W.make_x(w), W.make_logits(w), W.expert_scale(w)
+    f = run_stages(x, lg, s, w.k, w.R, w.C, w.dtype == W.DTYPE_FP8_E4M3_B128, fused=True)
+    for key in ["topk_idx", "slot", "counts", "offsets", "rank_counts", "out"]:
+        assert np.array_equal(np.asarray(f[key]), np.asarray(g[key])), key
