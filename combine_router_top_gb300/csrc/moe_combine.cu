@@ -40,12 +40,14 @@ __device__ __forceinline__ int load_choice(unsigned t, int k, int C, const int32
     return s >= 0 ? e * C + s : -1;
 }
 
-// Unit = (token, 32 consecutive 16-byte chunks of its row): lane l owns chunk
-// 32*seg + l. The warp broadcasts each kept choice (ascending j) by shuffle,
-// issues all gathers, then accumulates in fp32 in ascending j. The next
-// unit's routing is loaded before the current unit's gathers are issued.
-template <int KMAX>
-__global__ void __launch_bounds__(kBlock, KMAX <= 8 ? 4 : 2)
+// Unit = (token, 32*U consecutive 16-byte chunks of its row): lane l owns
+// chunks 32*(U*seg + i) + l, i < U. The warp broadcasts each kept choice
+// (ascending j) by shuffle, issues all KMAX*U gathers, then accumulates each
+// chunk in fp32 in ascending j. U > 1 for small k keeps as many loads in
+// flight per lane as top-8 has. The next unit's routing is loaded before the
+// current unit's gathers are issued.
+template <int KMAX, int U>
+__global__ void __launch_bounds__(kBlock, KMAX * U <= 8 ? 4 : 2)
 combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ topk_idx,
                const float *__restrict__ topk_w, const int32_t *__restrict__ slot,
                uint4 *__restrict__ out, int T, int H8, int k, int C, int segs) {
@@ -62,43 +64,55 @@ combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ topk_idx
         float nwt = 0.0f;
         int nrow = -1;
         if (more) nrow = load_choice(nw.row, k, C, topk_idx, topk_w, slot, nwt);
-        const unsigned c = wk.seg * 32 + lane;
-        const bool on = c < (unsigned)H8;
+        const unsigned c0 = wk.seg * (32 * U) + lane;
         const unsigned kept = __ballot_sync(kFull, src_row >= 0);
         const int n_kept = __popc(kept);
-        uint4 v[KMAX];
+        uint4 v[KMAX][U];
         unsigned rem = kept;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             if (j < n_kept) {                                  // warp-uniform
                 const int src = __ffs(rem) - 1;
                 rem &= rem - 1;
-                const size_t row = (size_t)__shfl_sync(kFull, src_row, src);
-                if (on) v[j] = ld_stream_v4(y + row * H8 + c);
+                const uint4 *yr = y + (size_t)__shfl_sync(kFull, src_row, src) * H8;
+#pragma unroll
+                for (int i = 0; i < U; ++i)
+                    if (c0 + 32 * i < (unsigned)H8) v[j][i] = ld_stream_v4(yr + c0 + 32 * i);
             }
         }
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        float wj[KMAX];
         rem = kept;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
+            wj[j] = 0.0f;
             if (j < n_kept) {                                  // warp-uniform
                 const int src = __ffs(rem) - 1;
                 rem &= rem - 1;
-                const float wj = __shfl_sync(kFull, w, src);
-                const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = __fmaf_rn(wj, bf16_lo(wv[i]), acc[2 * i]);
-                    acc[2 * i + 1] = __fmaf_rn(wj, bf16_hi(wv[i]), acc[2 * i + 1]);
-                }
+                wj[j] = __shfl_sync(kFull, w, src);
             }
         }
-        if (on)
-            st_v4(out + (size_t)wk.row * H8 + c,
-                  make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) {
+                if (j < n_kept) {                              // warp-uniform
+                    const uint32_t wv[4] = {v[j][i].x, v[j][i].y, v[j][i].z, v[j][i].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = __fmaf_rn(wj[j], bf16_lo(wv[q]), acc[2 * q]);
+                        acc[2 * q + 1] = __fmaf_rn(wj[j], bf16_hi(wv[q]), acc[2 * q + 1]);
+                    }
+                }
+            }
+            const unsigned c = c0 + 32 * i;
+            if (c < (unsigned)H8)
+                st_v4(out + (size_t)wk.row * H8 + c,
+                      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                 pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+        }
         if (!more) break;
         wk = nw;
         src_row = nrow;
@@ -285,18 +299,18 @@ extern "C" int moe_expert_synthetic(const moe_problem *p, const void *recv, cons
 }
 
 namespace {
-template <int KMAX>
+template <int KMAX, int U = (KMAX < 8 ? 8 / KMAX : 1)>
 int launch_combine(const moe::Dims &d, cudaStream_t st, const uint4 *y, const int32_t *idx, const float *w,
                    const int32_t *slot, uint4 *out) {
     using namespace moe;
     static PerContext<int> resident_cache;
-    const int resident = resident_blocks_cached(resident_cache, combine_kernel<KMAX>, kBlock);
+    const int resident = resident_blocks_cached(resident_cache, combine_kernel<KMAX, U>, kBlock);
     const int H8 = d.H / 8;
-    const int segs = (H8 + 31) / 32;
+    const int segs = (H8 + 32 * U - 1) / (32 * U);
     const long long units = (long long)d.T * segs;
     if (units >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
     const int grid = persistent_grid((units + kWarps - 1) / kWarps, resident, d.max_blocks);
-    if (launch_pdl(combine_kernel<KMAX>, grid, kBlock, st, y, idx, w, slot, out, d.T, H8, d.k, d.C, segs) !=
+    if (launch_pdl(combine_kernel<KMAX, U>, grid, kBlock, st, y, idx, w, slot, out, d.T, H8, d.k, d.C, segs) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
