@@ -776,9 +776,11 @@ def run_ours(args, rank: int, world: int, local: int):
     return line, dev
 
 
-def run_all_configs(args, dev, reps: int = 20) -> dict:
+def run_all_configs(args, dev, reps: int = 100) -> dict:
     """Route, dispatch, expert stand-in and combine of every configuration,
-    each call isolated (L2 flushed before it) and event-timed on its stream;
+    each call isolated (L2 flushed before it) and event-timed on its stream,
+    the mean of `reps` calls (one event interval is quantised to a fraction of
+    a microsecond, so a median of few calls is off by up to half a step);
     the dual-batch configuration is timed per micro-batch (half its tokens).
     Parity of each configuration is the GPU test suite's, not this run's."""
     import torch
@@ -823,7 +825,7 @@ def run_all_configs(args, dev, reps: int = 20) -> dict:
         kept = w.T * w.k - int(b["dropped"].item())
         by = {"route": bytes_route(w), "dispatch": bytes_dispatch(w, kept), "expert": bytes_expert(w, kept),
               "combine": bytes_combine(w, kept)}
-        us = {n: 1e3 * statistics.median(a.elapsed_time(z) for a, z in v) for n, v in times.items()}
+        us = {n: 1e3 * statistics.fmean(a.elapsed_time(z) for a, z in v) for n, v in times.items()}
         row = {"workload": name if name != "dbo" else "dbo (one micro-batch)", "T": w.T, "H": w.H, "E": w.E,
                "top_k": w.k, "R": w.R, "C": w.C,
                "dispatch_dtype": "fp8_e4m3_b128" if w.dtype == W.DTYPE_FP8_E4M3_B128 else "bf16",
@@ -835,7 +837,7 @@ def run_all_configs(args, dev, reps: int = 20) -> dict:
         rows.append(row)
         del b, x, out
         torch.cuda.empty_cache()
-    return {"peak_gbs": peak, "peak_source": f"{peak_kind} hbm_gbs", "reps": reps,
+    return {"peak_gbs": peak, "peak_source": f"{peak_kind} hbm_gbs", "reps": reps, "statistic": "mean",
             "l2": "flushed before every call", "configs": rows}
 
 
