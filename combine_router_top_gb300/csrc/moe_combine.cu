@@ -10,8 +10,9 @@
 // Both kernels are persistent: one wave of resident thread blocks walks a
 // list of small work units, so that no partial second wave idles SMs, and
 // no block-wide barrier sits in the steady-state loop.
-//   combine: every warp walks its own units (token, 32 chunks of 16 bytes);
-//     the routing of a token is held by lanes j < k and broadcast by shuffle.
+//   combine: every warp walks its own units (token, 32*U chunks of 16 bytes,
+//     U = 4, 2 or 1 for top-2, top-4 and above); the routing of a token is
+//     held by lanes j < k and broadcast by shuffle.
 //   expert: tasks (kept row, 16-byte piece) are numbered over the kept rows
 //     only, through an exclusive scan of min(counts[e], C) held in shared
 //     memory, so no thread walks empty capacity rows; the fp8 expert writes
