@@ -46,15 +46,25 @@ def test_workload_parity(name):
     compare(g, o, w.C, w.dtype == W.DTYPE_FP8_E4M3_B128)
 
 
+GRID_CASES = {
+    "fp8_top8": W.WORKLOADS["dsv3_fp8"].with_(T=300),
+    # combine units of 4 and 2 chunk groups (top-2, top-4), rows ragged against them
+    "bf16_top2": W.WORKLOADS["mixtral_skew"].with_(T=300, H=1800, C=400),
+    "bf16_top4": W.WORKLOADS["v2lite"].with_(T=300, k=4, H=2056),
+}
+
+
 @pytest.mark.parametrize("max_blocks", [1, 7, 152, 1000])
-def test_results_do_not_depend_on_the_grid(max_blocks):
+@pytest.mark.parametrize("case", list(GRID_CASES))
+def test_results_do_not_depend_on_the_grid(case, max_blocks):
     """Capped grids (grid-stride loops, as the overlapped kernels of the
     dual-batch step use) give bit-identical results."""
     from gpu_path import run_stages
-    w = W.WORKLOADS["dsv3_fp8"].with_(T=300)
+    w = GRID_CASES[case]
+    fp8 = w.dtype == W.DTYPE_FP8_E4M3_B128
     x, lg, s = W.make_x(w), W.make_logits(w), W.expert_scale(w)
-    a = run_stages(x, lg, s, w.k, w.R, w.C, True)
-    b = run_stages(x, lg, s, w.k, w.R, w.C, True, max_blocks=max_blocks)
+    a = run_stages(x, lg, s, w.k, w.R, w.C, fp8)
+    b = run_stages(x, lg, s, w.k, w.R, w.C, fp8, max_blocks=max_blocks)
     for key in a:
         assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
 
