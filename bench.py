@@ -776,6 +776,9 @@ def run_ours(args, rank: int, world: int, local: int):
     return line, dev
 
 
+ALL_CONFIGS = ["tiny", "v2lite", "mixtral_skew", "dsv3_fp8", "dbo"]
+
+
 def run_all_configs(args, dev, reps: int = 100) -> dict:
     """Route, dispatch, expert stand-in and combine of every configuration,
     each call isolated (L2 flushed before it) and event-timed on its stream,
@@ -791,7 +794,9 @@ def run_all_configs(args, dev, reps: int = 100) -> dict:
     flush_r = torch.ones_like(flush_w)
     stream = torch.cuda.current_stream()
     rows = []
-    for name in ["tiny", "v2lite", "mixtral_skew", "dsv3_fp8", "dbo"]:
+    for name in ALL_CONFIGS:
+        if args.only is not None and name != args.only:
+            continue
         w = W.WORKLOADS[name]
         if name == "dbo":
             w = w.with_(T=w.T // 2)
@@ -1173,6 +1178,8 @@ def main():
     ap.add_argument("--dbo-only", action="store_true", help="only the dual-batch-overlap measurements")
     ap.add_argument("--all-configs", action="store_true",
                     help="only the per-configuration timings of route, dispatch, expert and combine")
+    ap.add_argument("--only", choices=ALL_CONFIGS, default=None,
+                    help="with --all-configs: this configuration alone")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
