@@ -6,6 +6,7 @@ test, an inclusive scan, rounding that truncates, a dropped term...),
 compiles the copy, and runs the oracle's pin tests against it in a fresh
 process. Every mutant must make at least one pin fail. All on the CPU.
 """
+import concurrent.futures
 import os
 import subprocess
 import sys
@@ -111,14 +112,16 @@ MUTANTS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_catch_planted_mistake(name, tmp_path):
+def _run_mutant(name, workdir):
+    """Compile the oracle with mutant `name` planted and run the pin tests
+    against it in a fresh process: (site found, return code, stdout)."""
     src = open(SRC).read()
     before, after = MUTANTS[name]
-    assert src.count(before) >= 1, f"mutation site of {name} not found: the oracle changed"
+    if src.count(before) < 1:
+        return False, None, ""
     mutated = src.replace(before, after, 1)
-    c_path = tmp_path / "moe_oracle_mutant.c"
-    so_path = tmp_path / "liboracle_mutant.so"
+    c_path = workdir / f"{name}.c"
+    so_path = workdir / f"lib{name}.so"
     c_path.write_text(mutated)
     subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
                     "-o", str(so_path), str(c_path), "-lm"], check=True, capture_output=True)
@@ -127,6 +130,23 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_codecs.py"),
                         os.path.join(ROOT, "tests", "test_oracle_path.py"),
                         os.path.join(ROOT, "tests", "test_oracle_gemm.py")],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, f"no pin caught mutant {name}:\n{r.stdout[-2000:]}"
-    assert "failed" in r.stdout
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    return True, r.returncode, r.stdout
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    """Every mutant's pin run, several at a time (each is its own process)."""
+    workdir = tmp_path_factory.mktemp("mutants")
+    names = sorted(MUTANTS)
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        return dict(zip(names, ex.map(lambda n: _run_mutant(n, workdir), names)))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, mutant_results):
+    found, returncode, stdout = mutant_results[name]
+    assert found, f"mutation site of {name} not found: the oracle changed"
+    assert returncode != 0, f"no pin caught mutant {name}:\n{stdout[-2000:]}"
+    assert "failed" in stdout
